@@ -1,0 +1,430 @@
+"""Benchmark of the group-wise affine-quantized multi-row matmul on GB300.
+
+Workload (MLP up-projection shape): K=5120, N=17408, 4-bit codes, group 32,
+bf16 out, M in {1, 2, 4, 8, 16} rows. One step = 40 qmm_forward calls: every
+M on each of 8 independent weight copies (8 x 55.7 MB = 446 MB > 3x the 129 MB
+L2), in a fixed rotation so no call reads weights the previous call touched.
+Inputs are seeded synthetic data (datagen), resident in HBM before timing.
+
+Metric: effective HBM GB/s = (packed codes + fp16 scales + fp16 biases + bf16 x
++ bf16 y) bytes / time, plus us/call and GB/s per M.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qmm|reference]
+
+--impl reference times the CPU oracle (float64 C++) on the same workload (a
+bounded sample per step). Under torchrun each rank runs an independent replica
+(the op has no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import datagen  # noqa: E402
+
+WORKLOAD = "mlp_up"
+MS = [1, 2, 4, 8, 16]
+COPIES = 8
+METRIC = "qmm effective HBM GB/s (codes+scales+biases+x+y bytes / time), M=1,2,4,8,16"
+
+# DRAM bytes per main-kernel launch measured with ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum) on this workload, keyed by M, and the hash of the
+# kernel sources they were measured on. If the sources change, traffic is
+# reported as null until re-measured.
+TRAFFIC = {"source_sha": None, "per_M": {}}
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_affine_quantized_group_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def algorithmic_bytes(M: int, K: int, N: int, bits: int, group: int, out_bytes: int) -> int:
+    codes = N * K * bits // 8
+    sb = N * (K // group) * 2 * 2
+    return codes + sb + M * K * 2 + M * N * out_bytes
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# distributed (replicas only: barrier + max of the timed region)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws: int, backend: str):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def aggregate(dist, value_local_units: float, seconds_local: float):
+    """Whole-job throughput: units summed over ranks / max time over ranks."""
+    if dist is None:
+        return value_local_units, seconds_local
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([seconds_local], dtype=torch.float64, device=dev)
+    u = torch.tensor([value_local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(u.item()), float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        # "under load": samples within 30% of the highest observed clock (idle gaps excluded)
+        top = max(sm) if sm else 0.0
+        load = [v for v in sm if v >= 0.7 * top] or sm
+        return {"sm_mhz": float(np.median(load)) if load else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, ws, rank, local):
+    import torch
+    from bit_affine_quantized_group_gb300 import _build
+    _build.build()
+    import bit_affine_quantized_group_gb300 as q
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = dist_init(ws, "nccl")
+    wl = datagen.WORKLOADS[WORKLOAD]
+    K, N, bits, group = wl["K"], wl["N"], 4, wl["group"]
+
+    inp = datagen.gen_qmm(datagen.workload_seed(WORKLOAD), 16, K, N, bits, group, banks=COPIES)
+    x_host = inp.x
+    x = torch.from_numpy(x_host.view(np.int16)).to(dev).view(torch.bfloat16)
+    W = [torch.from_numpy(inp.words[i].view(np.int32)).to(dev) for i in range(COPIES)]
+    S = [torch.from_numpy(inp.scales[i].view(np.int16)).to(dev).view(torch.float16) for i in range(COPIES)]
+    B = [torch.from_numpy(inp.biases[i].view(np.int16)).to(dev).view(torch.float16) for i in range(COPIES)]
+    del inp
+    plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="bf16", splits=0, device=dev)
+    info = plan.info()
+    outs = {M: torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in MS}
+    kernels_per_call = 2 + (1 if info["splits"] > 1 else 0)
+
+    # one step: call j uses M = MS[j % 5] and weight copy j % 8 (all 40 pairs)
+    calls = [(MS[j % len(MS)], j % COPIES) for j in range(len(MS) * COPIES)]
+    step_bytes = sum(algorithmic_bytes(M, K, N, bits, group, 2) for M, _ in calls)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(call_list):
+        for M, c in call_list:
+            q.forward(plan, x[:M], W[c], S[c], B[c], outs[M], stream=stream)
+
+    def timed(call_list, steps, warmup, use_graph):
+        with torch.cuda.stream(stream):
+            for _ in range(max(warmup, 3)):
+                step(call_list)
+        torch.cuda.synchronize()
+        graph = None
+        if use_graph:
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    step(call_list)
+                torch.cuda.synchronize()
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        graph.replay()
+                torch.cuda.synchronize()
+            except Exception as e:   # capture unsupported: time direct launches
+                sys.stderr.write(f"graph capture failed ({e}); timing direct launches\n")
+                graph = None
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                if graph is not None:
+                    graph.replay()
+                else:
+                    step(call_list)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        return e0.elapsed_time(e1) / 1e3, graph is not None
+
+    peaks = load_peaks()
+    use_graph = not args.no_graph
+
+    # per-M loops (8 calls, one per weight copy)
+    per_m = {}
+    for M in MS:
+        cl = [(M, c) for c in range(COPIES)]
+        reps = max(20, args.steps // 4)
+        sec, _ = timed(cl, reps, args.warmup, use_graph)
+        us = sec / (reps * COPIES) * 1e6
+        gbs = algorithmic_bytes(M, K, N, bits, group, 2) / (us * 1e-6) / 1e9
+        per_m[str(M)] = {"us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                         "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+    # headline: K steps of the full 40-call sweep, clocks sampled meanwhile
+    clocks = ClockSampler(local)
+    clocks.start()
+    sec, graphed = timed(calls, args.steps, args.warmup, use_graph)
+    clk = clocks.stop()
+    units_local = step_bytes * args.steps / 1e9
+    units, sec_max = aggregate(dist, units_local, sec)
+    value = units / sec_max
+    ms_per_step = sec_max / args.steps * 1e3
+
+    # end to end through the public call with host buffers: pinned x in, pinned y out
+    x_pin = torch.from_numpy(x_host.view(np.int16)).pin_memory()
+    x_dev = torch.empty((16, K), dtype=torch.int16, device=dev)
+    y_pin = {M: torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for M in MS}
+    e2e_steps = max(5, min(args.steps, 200))
+    h2d = sum(M * K * 2 for M, _ in calls)
+    d2h = sum(M * N * 2 for M, _ in calls)
+
+    def e2e_step():
+        for M, c in calls:
+            x_dev[:M].copy_(x_pin[:M], non_blocking=True)
+            q.forward(plan, x_dev[:M].view(torch.bfloat16), W[c], S[c], B[c], outs[M], stream=stream)
+            y_pin[M].copy_(outs[M], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            e2e_step()
+    stream.synchronize()
+    e2e_sec = time.perf_counter() - t0
+    e2e_units, e2e_max = aggregate(dist, step_bytes * e2e_steps / 1e9, e2e_sec)
+    e2e_value = e2e_units / e2e_max
+
+    flags = plan.error_flags()
+    if flags != 0:
+        raise RuntimeError(f"kernel reported a bounded-wait timeout (flags={flags})")
+
+    if rank != 0:
+        return
+    traffic = None
+    if TRAFFIC["source_sha"] == kernel_source_sha() and TRAFFIC["per_M"]:
+        traffic = float(np.mean([TRAFFIC["per_M"][str(M)] for M in MS]))
+    cpu = cpu_baseline(K, N, bits, group) if ws == 1 else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded: uniform codes, fp16 scales U[0.002,0.02], biases -8*s+N(0,1e-3), x~N(0,1) bf16)",
+        "config": {"workload": f"{WORKLOAD}: K={K} N={N} bits={bits} group={group} out=bf16 M=1,2,4,8,16",
+                   "calls_per_step": len(calls), "weight_copies": COPIES,
+                   "l2": f"inputs larger than L2: {COPIES} rotating weight copies "
+                         f"({COPIES * algorithmic_bytes(0, K, N, bits, group, 0) / 1e6:.0f} MB > 3x 129 MB L2)",
+                   "launch": "cuda_graph" if graphed else "direct", "splits": info["splits"],
+                   "stages": info["stages"], "parallelism": f"replicas x{ws}", "accumulate": "fp32"},
+        "per_M": per_m,
+        "roofline": {"bound": "hbm", "achieved": round(value / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(value / ws / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "peak_source": peaks["source"], "kernel": "qmm_main_kernel (timed with its staging kernel)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "launch": "direct"},
+        "gpu_launches": kernels_per_call * len(calls) * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reported baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(K, N, bits, group, ncols):
+    """One bounded sample of the workload on the oracle: every M, `ncols`
+    output columns. Returns (seconds, algorithmic bytes of that sample)."""
+    import oracle
+    oracle.build()
+    inp = datagen.gen_qmm(datagen.workload_seed(WORKLOAD), 16, K, N, bits, group)
+    cols = np.arange(ncols, dtype=np.int64)
+    frac = ncols / N
+    t0 = time.perf_counter()
+    for M in MS:
+        oracle.qmm_f64_cols(inp.x[:M], inp.words[0], inp.scales[0], inp.biases[0], K, N, bits, group, cols)
+    sec = time.perf_counter() - t0
+    nbytes = sum(int(algorithmic_bytes(M, K, N, bits, group, 2) * frac) for M in MS)
+    return sec, nbytes
+
+
+def cpu_baseline(K, N, bits, group):
+    import oracle
+    oracle.build()
+    ncols = N
+    total_sec, total_bytes, runs = 0.0, 0, 0
+    while total_sec < 10.0 and runs < 50:
+        sec, nb = oracle_sample(K, N, bits, group, ncols)
+        total_sec += sec
+        total_bytes += nb
+        runs += 1
+    return {"value": round(total_bytes / total_sec / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{runs} full sweeps of M=1,2,4,8,16 over all {N} columns ({total_sec:.1f} s)"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = datagen.WORKLOADS[WORKLOAD]
+    K, N, bits, group = wl["K"], wl["N"], 4, wl["group"]
+    # bounded sample per step: all M values on the first `ncols` output columns,
+    # sized so that warmup + steps take about 90 s of oracle time in total
+    t_cal, _ = oracle_sample(K, N, bits, group, 256)
+    per_step = min(3.0, 90.0 / max(1, args.steps + args.warmup))
+    ncols = int(256 * per_step / max(t_cal, 1e-6)) // 16 * 16
+    ncols = max(16, min(N, ncols))
+    for _ in range(args.warmup):
+        oracle_sample(K, N, bits, group, ncols)
+    tot_sec, tot_bytes = 0.0, 0
+    for _ in range(args.steps):
+        sec, nb = oracle_sample(K, N, bits, group, ncols)
+        tot_sec += sec
+        tot_bytes += nb
+    value = tot_bytes / tot_sec / 1e9
+    sample = f"per step: M=1,2,4,8,16 on {ncols} of {N} output columns (bytes scaled to the sample)"
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(tot_sec / max(1, args.steps) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": f"{WORKLOAD}: K={K} N={N} bits={bits} group={group} out=bf16 M=1,2,4,8,16",
+                   "parallelism": "CPU oracle, OpenMP over columns"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
+    ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA graph replay")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    run_gpu(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,347 @@
+// C ABI of the qmm library: descriptor validation, plans, and the forward
+// dispatch. Declarations and the contract are in include/qmm.h.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "../../include/qmm.h"
+#include "qmm_kernels.cuh"
+
+using namespace qmmk;
+
+static_assert(QMM_MAX_BANKS == kMaxBanks, "bank table size");
+
+struct qmm_plan {
+    qmm_desc d;
+    int device;
+    int num_sms;
+    int splits;
+    int C;
+    int G;
+    int stages[2];       // index 0: M <= 8 (MB = 8), 1: M > 8 (MB = 16)
+    int smem[2];
+    uint8_t* ws;
+    size_t ws_bytes;
+    bool owns_ws;
+    uint32_t* err;       // device error word (start of the workspace)
+    uint8_t* xprep;
+    float* partial;
+};
+
+namespace {
+
+constexpr size_t kErrBytes = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int chunks_of(const qmm_desc* d) {
+    const int64_t G = d->K / d->group;
+    return static_cast<int>((G + kGPC - 1) / kGPC);
+}
+
+// Largest K-slice count a plan for d may use (the automatic choice never exceeds it).
+int splits_cap(const qmm_desc* d) {
+    if (d->splits > 0) return d->splits;
+    int c = chunks_of(d) / 3;
+    if (c < 1) c = 1;
+    if (c > 8) c = 8;
+    return c;
+}
+
+// Automatic K-slice count: enough (bank, slice, row) work for ~96 rows per SM,
+// at least 3 chunks per slice, at most 8 slices.
+int auto_splits(const qmm_desc* d, int num_sms) {
+    const int C = chunks_of(d);
+    int s = 1;
+    while (d->N * s < 96LL * num_sms && s < 8 && (s + 1) * 3 <= C) ++s;
+    return s;
+}
+
+int mb_index(int M) { return M > 8 ? 1 : 0; }
+int max_mb(const qmm_desc* d) { return d->max_M > 8 ? 16 : 8; }
+
+size_t xprep_region_bytes(const qmm_desc* d) {
+    return static_cast<size_t>(chunks_of(d)) *
+           static_cast<size_t>(xprep_chunk_bytes(d->bits, d->group, max_mb(d)));
+}
+
+size_t partial_region_bytes(const qmm_desc* d, int splits) {
+    if (splits <= 1) return 0;
+    return static_cast<size_t>(d->max_banks) * splits * d->max_M * static_cast<size_t>(d->N) * sizeof(float);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+cudaError_t configure(int bits, int group, int mb, int smem) {
+    switch (bits) {
+        case 4: return configure_kernels<4>(group, mb, smem);
+        case 5: return configure_kernels<5>(group, mb, smem);
+        case 6: return configure_kernels<6>(group, mb, smem);
+        case 8: return configure_kernels<8>(group, mb, smem);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch(int bits, int group, const LaunchCfg& L, const MainParams& mp) {
+    switch (bits) {
+        case 4: return launch_forward<4>(group, L, mp);
+        case 5: return launch_forward<5>(group, L, mp);
+        case 6: return launch_forward<6>(group, L, mp);
+        case 8: return launch_forward<8>(group, L, mp);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qmm_status_string(int status) {
+    switch (status) {
+        case QMM_OK: return "QMM_OK";
+        case QMM_ERR_INVALID_ARG: return "QMM_ERR_INVALID_ARG: invalid argument";
+        case QMM_ERR_UNSUPPORTED: return "QMM_ERR_UNSUPPORTED: format or shape not supported";
+        case QMM_ERR_PLAN_MISMATCH: return "QMM_ERR_PLAN_MISMATCH: K/N/bits/group differ from the plan";
+        case QMM_ERR_CUDA: return "QMM_ERR_CUDA: CUDA runtime error";
+        case QMM_ERR_ALLOC: return "QMM_ERR_ALLOC: allocation failed";
+        case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        default: return "unknown qmm status";
+    }
+}
+
+int qmm_validate_desc(const qmm_desc* d) {
+    if (d == nullptr) return QMM_ERR_INVALID_ARG;
+    if (d->K <= 0 || d->N <= 0 || d->group <= 0 || d->bits <= 0) return QMM_ERR_INVALID_ARG;
+    if (d->K > (1LL << 24) || d->N > (1LL << 30)) return QMM_ERR_INVALID_ARG;
+    if (d->K % d->group != 0) return QMM_ERR_INVALID_ARG;
+    if (d->max_M < 1 || d->max_M > QMM_MAX_ROWS) return QMM_ERR_INVALID_ARG;
+    if (d->out_dtype != QMM_OUT_F32 && d->out_dtype != QMM_OUT_BF16) return QMM_ERR_INVALID_ARG;
+    if (d->splits < 0 || d->splits > QMM_MAX_SPLITS) return QMM_ERR_INVALID_ARG;
+    if (d->max_banks < 1 || d->max_banks > QMM_MAX_BANKS) return QMM_ERR_INVALID_ARG;
+    if (d->bits != 4 && d->bits != 5 && d->bits != 6 && d->bits != 8) return QMM_ERR_UNSUPPORTED;
+    if (d->group != 32 && d->group != 64) return QMM_ERR_UNSUPPORTED;
+    if ((d->K * d->bits) % 128 != 0) return QMM_ERR_UNSUPPORTED;
+    if ((d->K / d->group) % 2 != 0) return QMM_ERR_UNSUPPORTED;
+    if (d->splits > chunks_of(d)) return QMM_ERR_UNSUPPORTED;
+    return QMM_OK;
+}
+
+size_t qmm_workspace_bytes(const qmm_desc* d) {
+    if (qmm_validate_desc(d) != QMM_OK) return 0;
+    return kErrBytes + align_up(xprep_region_bytes(d), 256) + partial_region_bytes(d, splits_cap(d));
+}
+
+int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_bytes) {
+    if (plan == nullptr) return QMM_ERR_INVALID_ARG;
+    *plan = nullptr;
+    const int v = qmm_validate_desc(d);
+    if (v != QMM_OK) return v;
+    const size_t need = qmm_workspace_bytes(d);
+    if (workspace != nullptr && (ws_bytes < need || !aligned(workspace, 256))) return QMM_ERR_INVALID_ARG;
+
+    int dev = 0, sms = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QMM_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return QMM_ERR_CUDA;
+
+    struct qmm_plan* p = new (std::nothrow) struct qmm_plan();
+    if (p == nullptr) return QMM_ERR_ALLOC;
+    p->d = *d;
+    p->device = dev;
+    p->num_sms = sms;
+    p->C = chunks_of(d);
+    p->G = static_cast<int>(d->K / d->group);
+    p->splits = d->splits > 0 ? d->splits : auto_splits(d, sms);
+    if (p->splits > splits_cap(d)) p->splits = splits_cap(d);
+
+    const int nmb = d->max_M > 8 ? 2 : 1;
+    for (int i = 0; i < 2; ++i) {
+        p->stages[i] = 0;
+        p->smem[i] = 0;
+    }
+    for (int i = 0; i < nmb; ++i) {
+        const int mb = i == 0 ? 8 : 16;
+        const int sb = stage_bytes(d->bits, d->group, mb);
+        int st = (optin - 1024) / (sb + 16);
+        if (st > kMaxStages) st = kMaxStages;
+        if (st < 2) {
+            delete p;
+            return QMM_ERR_UNSUPPORTED;
+        }
+        p->stages[i] = st;
+        p->smem[i] = st * sb + st * 16;
+        if (configure(d->bits, d->group, mb, p->smem[i]) != cudaSuccess) {
+            delete p;
+            return QMM_ERR_CUDA;
+        }
+    }
+
+    if (workspace == nullptr) {
+        void* ws = nullptr;
+        if (cudaMalloc(&ws, need) != cudaSuccess) {
+            delete p;
+            return QMM_ERR_ALLOC;
+        }
+        p->ws = static_cast<uint8_t*>(ws);
+        p->ws_bytes = need;
+        p->owns_ws = true;
+    } else {
+        p->ws = static_cast<uint8_t*>(workspace);
+        p->ws_bytes = ws_bytes;
+        p->owns_ws = false;
+    }
+    p->err = reinterpret_cast<uint32_t*>(p->ws);
+    p->xprep = p->ws + kErrBytes;
+    p->partial = reinterpret_cast<float*>(p->ws + kErrBytes + align_up(xprep_region_bytes(d), 256));
+    if (cudaMemsetAsync(p->ws, 0, kErrBytes, 0) != cudaSuccess || cudaStreamSynchronize(0) != cudaSuccess) {
+        if (p->owns_ws) cudaFree(p->ws);
+        delete p;
+        return QMM_ERR_CUDA;
+    }
+    *plan = p;
+    return QMM_OK;
+}
+
+int qmm_plan_get_info(const qmm_plan_t* p, qmm_plan_info* info) {
+    if (p == nullptr || info == nullptr) return QMM_ERR_INVALID_ARG;
+    info->splits = p->splits;
+    info->chunks = p->C;
+    info->stages[0] = p->stages[0];
+    info->stages[1] = p->stages[1];
+    info->smem_bytes[0] = p->smem[0];
+    info->smem_bytes[1] = p->smem[1];
+    info->num_sms = p->num_sms;
+    info->device = p->device;
+    info->workspace_bytes = static_cast<int64_t>(p->ws_bytes);
+    return QMM_OK;
+}
+
+int qmm_check_forward_args(const qmm_desc* d, const void* x_bf16, int M, int n_banks,
+                           const uint32_t* const* packed_w, const uint16_t* const* scales_f16,
+                           const uint16_t* const* biases_f16, int64_t K, int64_t N, int bits, int group,
+                           void* const* out) {
+    if (d == nullptr) return QMM_ERR_INVALID_ARG;
+    if (K != d->K || N != d->N || bits != d->bits || group != d->group) return QMM_ERR_PLAN_MISMATCH;
+    if (M < 0 || M > d->max_M) return QMM_ERR_INVALID_ARG;
+    if (n_banks < 1 || n_banks > d->max_banks) return QMM_ERR_INVALID_ARG;
+    if (packed_w == nullptr || scales_f16 == nullptr || biases_f16 == nullptr || out == nullptr)
+        return QMM_ERR_INVALID_ARG;
+    if (M == 0) return QMM_OK;
+    if (x_bf16 == nullptr || !aligned(x_bf16, 2)) return QMM_ERR_INVALID_ARG;
+    const size_t sb_align = ((d->K / d->group) % 8 == 0) ? 16 : 4;
+    const size_t out_align = d->out_dtype == QMM_OUT_F32 ? 4 : 2;
+    for (int i = 0; i < n_banks; ++i) {
+        if (packed_w[i] == nullptr || !aligned(packed_w[i], 16)) return QMM_ERR_INVALID_ARG;
+        if (scales_f16[i] == nullptr || !aligned(scales_f16[i], sb_align)) return QMM_ERR_INVALID_ARG;
+        if (biases_f16[i] == nullptr || !aligned(biases_f16[i], sb_align)) return QMM_ERR_INVALID_ARG;
+        if (out[i] == nullptr || !aligned(out[i], out_align)) return QMM_ERR_INVALID_ARG;
+    }
+    return QMM_OK;
+}
+
+int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks,
+                       const uint32_t* const* packed_w, const uint16_t* const* scales_f16,
+                       const uint16_t* const* biases_f16, int64_t K, int64_t N, int bits, int group,
+                       void* const* out, void* stream) {
+    if (p == nullptr) return QMM_ERR_INVALID_ARG;
+    const int chk = qmm_check_forward_args(&p->d, x_bf16, M, n_banks, packed_w, scales_f16, biases_f16, K, N,
+                                           bits, group, out);
+    if (chk != QMM_OK) return chk;
+    if (M == 0) return QMM_OK;
+
+    const int mi = mb_index(M);
+    if (p->stages[mi] == 0) return QMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    MainParams mp;
+    std::memset(&mp, 0, sizeof(mp));
+    mp.xprep = p->xprep;
+    mp.partial = p->partial;
+    mp.err = p->err;
+    mp.N = N;
+    mp.K = K;
+    mp.row_bytes = K * bits / 8;
+    mp.G = p->G;
+    mp.C = p->C;
+    mp.splits = p->splits;
+    mp.M = M;
+    mp.stages = p->stages[mi];
+    mp.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
+    mp.sb_vec16 = (p->G % 8 == 0) ? 1 : 0;
+    mp.banks = n_banks;
+    mp.rows_total = static_cast<int64_t>(n_banks) * p->splits * N;
+    for (int i = 0; i < n_banks; ++i) {
+        mp.bank[i].w = packed_w[i];
+        mp.bank[i].s = scales_f16[i];
+        mp.bank[i].b = biases_f16[i];
+        mp.bank[i].out = out[i];
+    }
+    int64_t ctas = (mp.rows_total + kSlab - 1) / kSlab;
+    if (ctas > p->num_sms) ctas = p->num_sms;
+
+    LaunchCfg L;
+    L.x = static_cast<const uint16_t*>(x_bf16);
+    L.M = M;
+    L.mb = mi == 0 ? 8 : 16;
+    L.ctas = static_cast<int>(ctas);
+    L.smem = p->smem[mi];
+    L.stream = st;
+    if (launch(bits, group, L, mp) != cudaSuccess) return QMM_ERR_CUDA;
+
+    if (p->splits > 1) {
+        ReduceParams rp;
+        std::memset(&rp, 0, sizeof(rp));
+        rp.partial = p->partial;
+        rp.N = N;
+        rp.M = M;
+        rp.splits = p->splits;
+        rp.banks = n_banks;
+        rp.out_bf16 = p->d.out_dtype == QMM_OUT_BF16 ? 1 : 0;
+        for (int i = 0; i < n_banks; ++i) rp.out[i] = out[i];
+        if (launch_reduce(rp, static_cast<int64_t>(n_banks) * M * N, st) != cudaSuccess) return QMM_ERR_CUDA;
+    }
+    return QMM_OK;
+}
+
+int qmm_forward(const qmm_plan_t* p, const void* x_bf16, int M, const uint32_t* packed_w,
+                const uint16_t* scales_f16, const uint16_t* biases_f16, int64_t K, int64_t N, int bits, int group,
+                void* out, void* stream) {
+    return qmm_forward_banked(p, x_bf16, M, 1, &packed_w, &scales_f16, &biases_f16, K, N, bits, group, &out,
+                              stream);
+}
+
+int qmm_unpack_codes(const uint32_t* packed_w, int64_t K, int64_t N, int bits, uint8_t* codes, void* stream) {
+    if (bits != 4 && bits != 5 && bits != 6 && bits != 8) return QMM_ERR_UNSUPPORTED;
+    if (K <= 0 || N < 0 || K % 32 != 0 || K > (1LL << 24)) return QMM_ERR_INVALID_ARG;
+    if (N == 0) return QMM_OK;
+    if (packed_w == nullptr || codes == nullptr || !aligned(packed_w, 4)) return QMM_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (bits) {
+        case 4: e = launch_unpack<4>(packed_w, K, N, codes, st); break;
+        case 5: e = launch_unpack<5>(packed_w, K, N, codes, st); break;
+        case 6: e = launch_unpack<6>(packed_w, K, N, codes, st); break;
+        default: e = launch_unpack<8>(packed_w, K, N, codes, st); break;
+    }
+    return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+int qmm_plan_error(const qmm_plan_t* p, uint32_t* flags) {
+    if (p == nullptr || flags == nullptr) return QMM_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, p->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QMM_ERR_CUDA;
+    if (v != 0 && cudaMemset(p->err, 0, sizeof(v)) != cudaSuccess) return QMM_ERR_CUDA;
+    *flags = v;
+    return v == 0 ? QMM_OK : QMM_ERR_TIMEOUT;
+}
+
+void qmm_destroy(qmm_plan_t* p) {
+    if (p == nullptr) return;
+    if (p->owns_ws && p->ws != nullptr) cudaFree(p->ws);
+    delete p;
+}
+
+}  // extern "C"

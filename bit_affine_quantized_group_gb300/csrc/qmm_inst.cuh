@@ -1,0 +1,73 @@
+// Per-code-width launchers. Each qmm_inst_b<BITS>.cu includes this file with
+// QMM_INST_BITS defined, so the four widths compile as separate units.
+#pragma once
+
+#include "qmm_kernels.cuh"
+
+namespace qmmk {
+
+namespace {
+template <int BITS, int GROUP, int MB>
+cudaError_t configure_one(int smem_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+template <int BITS, int GROUP, int MB>
+cudaError_t launch_one(const LaunchCfg& L, const MainParams& mp) {
+    // (1) activation staging: ordinary stream order after the caller's work.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(mp.C));
+    cfg.blockDim = dim3(kXprepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_xprep_kernel<BITS, GROUP, MB>, L.x, L.M, mp.K, mp.G,
+                                       const_cast<uint8_t*>(mp.xprep));
+    if (e != cudaSuccess) return e;
+    // (2) main kernel as a programmatic dependent of (1).
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(L.ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB>, mp);
+}
+}  // namespace
+
+template <>
+cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, int smem_bytes) {
+    constexpr int B = QMM_INST_BITS;
+    if (group == 32) return mb == 8 ? configure_one<B, 32, 8>(smem_bytes) : configure_one<B, 32, 16>(smem_bytes);
+    if (group == 64) return mb == 8 ? configure_one<B, 64, 8>(smem_bytes) : configure_one<B, 64, 16>(smem_bytes);
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_forward<QMM_INST_BITS>(int group, const LaunchCfg& L, const MainParams& mp) {
+    constexpr int B = QMM_INST_BITS;
+    if (group == 32) return L.mb == 8 ? launch_one<B, 32, 8>(L, mp) : launch_one<B, 32, 16>(L, mp);
+    if (group == 64) return L.mb == 8 ? launch_one<B, 64, 8>(L, mp) : launch_one<B, 64, 16>(L, mp);
+    return cudaErrorInvalidValue;
+}
+
+template <>
+cudaError_t launch_unpack<QMM_INST_BITS>(const uint32_t* w, int64_t K, int64_t N, uint8_t* codes,
+                                          cudaStream_t stream) {
+    constexpr int B = QMM_INST_BITS;
+    const int64_t vbk = (B == 8) ? K / 16 : K / 32;
+    const int64_t total = N * vbk * 4;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    if (blocks < 1) blocks = 1;
+    qmm_unpack_kernel<B><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, K, N, codes);
+    return cudaGetLastError();
+}
+
+}  // namespace qmmk

@@ -1,0 +1,564 @@
+// qmm kernels for sm_103a.
+//
+// Per forward call, in stream order:
+//   1. qmm_xprep_kernel   -- stages x once per call: MMA B fragments in the
+//                            permuted k order the unpackers produce, the per-group
+//                            activation sums XS (the "b*XS" term of the
+//                            dequant-after-dot form, vmlx-swift PR #565, LaneQMM
+//                            commit) as split binary16 fragments, and one
+//                            power-of-two range factor per (row, chunk).
+//   2. qmm_main_kernel    -- one CTA per SM; a producer warp streams packed code
+//                            rows (1-D TMA bulk copies), scales and biases
+//                            (cp.async) and the staged activations into a ring of
+//                            shared-memory stages; four consumer warps unpack the
+//                            codes in registers and contract them on tensor cores,
+//                            reading each code byte once for all M rows (same
+//                            page, qwen_qmv_rows_full commit: weights read once per
+//                            k-block for all rows). Launched as a programmatic
+//                            dependent of (1): code loads start before (1) ends.
+//   3. qmm_splitk_reduce_kernel (splits > 1 only) -- sums the fp32 slice
+//                            partials in slice order (same page, "JANGH split-K
+//                            verify tile" commit: FP32 partials, then a sum).
+//
+// Per scale group g the main kernel forms, with 128-offset codes A = 128 + q,
+//   P'[m,n,g] = sum_{k in g} x[m,k] * A[n,k] = P + 128*XS
+// (for 8-bit codes, split into nibbles lo + 16*hi, P' = P + 2176*XS) and then
+//   y += s*P' + (b - OFF*s)*XS,      OFF = 128 (2176 for 8-bit),
+// which is  sum_g s*P + b*XS.  The s*P' part is one FMA per accumulator per
+// group; the (b, s) x (XS, -OFF*XS) part is a small binary16 MMA per 8-group
+// chunk, with XS split into high and low binary16 halves so it keeps ~22 bits.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "qmm_device.cuh"
+
+namespace qmmk {
+
+constexpr int kMaxBanks = 64;
+
+struct BankPtrs {
+    const uint32_t* w;
+    const uint16_t* s;
+    const uint16_t* b;
+    void* out;
+};
+
+enum OutMode : int { kOutF32 = 0, kOutBF16 = 1, kOutPartial = 2 };
+
+struct MainParams {
+    const uint8_t* xprep;   // per chunk: xprep_chunk_bytes(bits, group, MB)
+    float* partial;         // [banks][splits][M][N] when out_mode == kOutPartial
+    uint32_t* err;          // device error word
+    int64_t N;
+    int64_t K;
+    int64_t row_bytes;      // K*bits/8
+    int64_t rows_total;     // banks * splits * N
+    int G;                  // K / group
+    int C;                  // chunks = ceil(G / 8)
+    int splits;
+    int M;
+    int stages;
+    int out_mode;
+    int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
+    int banks;
+    BankPtrs bank[kMaxBanks];
+};
+
+struct ReduceParams {
+    const float* partial;
+    int64_t N;
+    int M;
+    int splits;
+    int banks;
+    int out_bf16;
+    void* out[kMaxBanks];
+};
+
+// ---------------------------------------------------------------------------
+// Work enumeration shared by the producer and the consumers: the flattened
+// (bank, split, row) space is cut evenly over the CTAs; a CTA's range is cut at
+// (bank, split) boundaries and then into balanced row blocks of <= kTN rows.
+// ---------------------------------------------------------------------------
+template <typename F>
+__device__ __forceinline__ void for_each_row_block(const MainParams& p, F&& f) {
+    const int64_t r_begin = p.rows_total * blockIdx.x / gridDim.x;
+    const int64_t r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
+    int64_t r = r_begin;
+    while (r < r_end) {
+        const int64_t seg = r / p.N;                                  // bank * splits + split
+        const int64_t seg_end = min(r_end, (seg + 1) * p.N);
+        const int64_t len = seg_end - r;
+        const int nb = static_cast<int>((len + kTN - 1) / kTN);
+        const int bank = static_cast<int>(seg / p.splits);
+        const int split = static_cast<int>(seg % p.splits);
+        const int c0 = static_cast<int>(static_cast<int64_t>(split) * p.C / p.splits);
+        const int c1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.C / p.splits);
+        for (int ib = 0; ib < nb; ++ib) {
+            const int64_t a = r + len * ib / nb;
+            const int64_t e = r + len * (ib + 1) / nb;
+            if (!f(bank, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
+        }
+        r = seg_end;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 1. Activation staging.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo, uint16_t hi) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+__device__ __forceinline__ uint16_t bf16_times16(uint16_t v) {
+    const float f = __bfloat162float(__ushort_as_bfloat16(v)) * 16.0f;   // exact (power of two)
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+    return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+}
+
+template <int BITS, int GROUP, int MB>
+__global__ void __launch_bounds__(kXprepThreads)
+qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_t* __restrict__ xprep) {
+    constexpr int CK = kGPC * GROUP;                 // codes per chunk
+    constexpr int KB = vblocks_per_chunk(BITS, GROUP);
+    constexpr int NT = n8_tiles(MB);
+    constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
+    constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
+    constexpr float OFF = code_offset(BITS);
+
+    // The main kernel may start loading weights while this runs.
+    griddep_launch_dependents();
+
+    __shared__ uint16_t xs[MB][CK];
+    __shared__ float xsum[MB][kGPC];
+    __shared__ float rsig[MB];     // 1 / sigma
+    __shared__ float sig[MB];
+
+    const int c = blockIdx.x;
+    const int g0 = c * kGPC;
+    const int ng = min(kGPC, G - g0);
+    const int64_t k0 = static_cast<int64_t>(g0) * GROUP;
+    const int kc = ng * GROUP;
+    const int tid = threadIdx.x;
+
+    for (int i = tid; i < MB * CK; i += blockDim.x) {
+        const int m = i / CK, k = i - (i / CK) * CK;
+        xs[m][k] = (m < M && k < kc) ? x[static_cast<int64_t>(m) * K + k0 + k] : static_cast<uint16_t>(0);
+    }
+    __syncthreads();
+    if (tid < MB * kGPC) {
+        const int m = tid / kGPC, gg = tid % kGPC;
+        float s = 0.0f;
+        for (int k = 0; k < GROUP; ++k) s += __bfloat162float(__ushort_as_bfloat16(xs[m][gg * GROUP + k]));
+        xsum[m][gg] = s;
+    }
+    __syncthreads();
+    if (tid < MB) {
+        float amax = 0.0f;
+        for (int gg = 0; gg < kGPC; ++gg) amax = fmaxf(amax, fabsf(xsum[tid][gg]));
+        amax *= OFF;
+        // sigma = 2^(e-13) puts the largest |OFF*XS/sigma| in [2^13, 2^14):
+        // inside the binary16 range with room to spare.
+        float sg = 1.0f;
+        if (amax > 0.0f && amax <= 3.0e38f) sg = ldexpf(1.0f, ilogbf(amax) - 13);
+        sig[tid] = sg;
+        rsig[tid] = 1.0f / sg;    // exact: power of two
+    }
+    __syncthreads();
+
+    uint8_t* out = xprep + static_cast<size_t>(c) * XPB;
+    uint4* frag = reinterpret_cast<uint4*>(out);
+    for (int i = tid; i < KB * NT * 32; i += blockDim.x) {
+        const int lane = i & 31;
+        const int j = (i >> 5) % NT;
+        const int vb = (i >> 5) / NT;
+        const int t = lane & 3;
+        const int m = 8 * j + (lane >> 2);
+        uint32_t r[4];
+        if constexpr (BITS == 8) {
+            // virtual block vb = real codes 16*vb .. 16*vb+15; lane t holds the
+            // word with real codes kb..kb+3; its nibble slots pair (lo q0, lo q2),
+            // (hi q0, hi q2), (lo q1, lo q3), (hi q1, hi q3); hi nibbles weigh 16.
+            const int kb = 16 * vb + 4 * t;
+            const uint16_t a0 = xs[m][kb], a1 = xs[m][kb + 1], a2 = xs[m][kb + 2], a3 = xs[m][kb + 3];
+            r[0] = pack_bf16x2(a0, a2);
+            r[1] = pack_bf16x2(bf16_times16(a0), bf16_times16(a2));
+            r[2] = pack_bf16x2(a1, a3);
+            r[3] = pack_bf16x2(bf16_times16(a1), bf16_times16(a3));
+        } else {
+            // lane t owns codes 8t..8t+7 of the k32 block; slot pair i is (c_i, c_{i+4}).
+            const int kb = 32 * vb + 8 * t;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) r[q] = pack_bf16x2(xs[m][kb + q], xs[m][kb + q + 4]);
+        }
+        frag[i] = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+    uint4* bias = reinterpret_cast<uint4*>(out + XFB);
+    for (int i = tid; i < NT * 32; i += blockDim.x) {
+        const int lane = i & 31;
+        const int j = i >> 5;
+        const int t = lane & 3;
+        const int m = 8 * j + (lane >> 2);
+        const float v0 = xsum[m][2 * t] * rsig[m];
+        const float v1 = xsum[m][2 * t + 1] * rsig[m];
+        const float w0 = -OFF * v0;
+        const float w1 = -OFF * v1;
+        const __half v0h = __float2half_rn(v0), v1h = __float2half_rn(v1);
+        const __half w0h = __float2half_rn(w0), w1h = __float2half_rn(w1);
+        const __half v0l = __float2half_rn(v0 - __half2float(v0h)), v1l = __float2half_rn(v1 - __half2float(v1h));
+        const __half w0l = __float2half_rn(w0 - __half2float(w0h)), w1l = __float2half_rn(w1 - __half2float(w1h));
+        bias[i] = make_uint4(pack_half2(v0h, v1h), pack_half2(w0h, w1h), pack_half2(v0l, v1l), pack_half2(w0l, w1l));
+    }
+    if (tid < MB) reinterpret_cast<float*>(out + XFB + xprep_bias_bytes(MB))[tid] = sig[tid];
+}
+
+// ---------------------------------------------------------------------------
+// 2. Main kernel.
+// ---------------------------------------------------------------------------
+template <int BITS, int GROUP, int MB>
+__global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_constant__ MainParams p) {
+    constexpr int VB = vblocks_per_group(BITS, GROUP);
+    constexpr int NT = n8_tiles(MB);
+    constexpr int BB = vblock_bytes(BITS);
+    constexpr int RS = chunk_row_stride(BITS, GROUP);
+    constexpr int RB = chunk_row_bytes(BITS, GROUP);
+    constexpr int SW = stage_weight_bytes(BITS, GROUP);
+    constexpr int SSB = stage_sb_bytes();
+    constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
+    constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
+    constexpr int SB = stage_bytes(BITS, GROUP, MB);
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+    uint64_t* empty = full + S;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1 + 32);      // producer lane 0 (expect_tx) + 32 cp.async arrivals
+            mbar_init(&empty[i], kNCW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    if (warp == kNCW) {
+        // ------------------------------ producer ------------------------------
+        const uint64_t pol = policy_evict_first();
+        uint32_t it = 0;
+        bool waited = false;
+        bool ok = true;
+        int npend = 0;
+        int pend_slot[kMaxStages];
+        int pend_chunk[kMaxStages];
+        auto flush_pending = [&]() {
+            griddep_wait();   // the staged activations of this call are ready
+            waited = true;
+            if (lane == 0)
+                for (int i = 0; i < npend; ++i)
+                    bulk_g2s(smem + pend_slot[i] * SB + SW + 2 * SSB, p.xprep + static_cast<size_t>(pend_chunk[i]) * XPB,
+                             XPB, &full[pend_slot[i]]);
+            npend = 0;
+        };
+        for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
+            (void)split;
+            const BankPtrs bp = p.bank[bank];
+            for (int c = c0; c < c1; ++c) {
+                const int slot = static_cast<int>(it % S);
+                if (it >= static_cast<uint32_t>(S) &&
+                    !mbar_wait(&empty[slot], ((it / S) - 1) & 1u, p.err, kErrEmptyWait)) {
+                    ok = false;
+                    return false;
+                }
+                const int ng = min(kGPC, p.G - c * kGPC);
+                const uint32_t wbytes = static_cast<uint32_t>(ng * GROUP * BITS / 8);
+                uint8_t* st = smem + slot * SB;
+                if (lane == 0) mbar_arrive_expect_tx(&full[slot], rows * wbytes + XPB);
+                __syncwarp();
+                const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(bp.w) + n0 * p.row_bytes +
+                                      static_cast<int64_t>(c) * RB;
+                for (int r = lane; r < rows; r += 32)
+                    bulk_g2s_stream(st + r * RS, wsrc + r * p.row_bytes, wbytes, &full[slot], pol);
+                uint8_t* sdst = st + SW;
+                uint8_t* bdst = sdst + SSB;
+                const uint16_t* ssrc = bp.s + n0 * p.G + c * kGPC;
+                const uint16_t* bsrc = bp.b + n0 * p.G + c * kGPC;
+                if (p.sb_vec16) {
+                    for (int r = lane; r < rows; r += 32) {
+                        cp_async_16(sdst + r * 16, ssrc + static_cast<int64_t>(r) * p.G);
+                        cp_async_16(bdst + r * 16, bsrc + static_cast<int64_t>(r) * p.G);
+                    }
+                } else {
+                    const int nq = ng >> 1;   // 4-byte pieces per row
+                    for (int i = lane; i < rows * nq; i += 32) {
+                        const int r = i / nq, q = i - (i / nq) * nq;
+                        cp_async_4(sdst + r * 16 + 4 * q, ssrc + static_cast<int64_t>(r) * p.G + 2 * q);
+                        cp_async_4(bdst + r * 16 + 4 * q, bsrc + static_cast<int64_t>(r) * p.G + 2 * q);
+                    }
+                }
+                cp_async_arrive_noinc(&full[slot]);
+                if (waited) {
+                    if (lane == 0)
+                        bulk_g2s(st + SW + 2 * SSB, p.xprep + static_cast<size_t>(c) * XPB, XPB, &full[slot]);
+                } else {
+                    pend_slot[npend] = slot;
+                    pend_chunk[npend] = c;
+                    if (++npend == S) flush_pending();
+                }
+                ++it;
+            }
+            return true;
+        });
+        if (!waited) flush_pending();
+        if (!ok) {
+            // Give the copies already issued a bounded chance to land before exiting.
+            const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0u;
+            for (uint32_t i = first; i < it; ++i)
+                if (!mbar_wait(&full[i % S], (i / S) & 1u, p.err, kErrDrainWait)) break;
+        }
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    uint32_t it = 0;
+    for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
+        const int nsl = (rows + kSlab - 1) / kSlab;
+        bool act[kSPW];
+        int row0[kSPW];
+#pragma unroll
+        for (int sw = 0; sw < kSPW; ++sw) {
+            const int slab = warp + sw * kNCW;
+            act[sw] = slab < nsl;
+            row0[sw] = slab * kSlab + g;
+        }
+        float acc[kSPW][NT][4];
+#pragma unroll
+        for (int sw = 0; sw < kSPW; ++sw)
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[sw][j][e] = 0.0f;
+
+        for (int c = c0; c < c1; ++c) {
+            const int slot = static_cast<int>(it % S);
+            if (!mbar_wait(&full[slot], (it / S) & 1u, p.err, kErrFullWait)) return false;
+            const int ng = min(kGPC, p.G - c * kGPC);
+            const uint8_t* st = smem + slot * SB;
+            const uint8_t* wst = st;
+            const uint16_t* sst = reinterpret_cast<const uint16_t*>(st + SW);
+            const uint16_t* bst = reinterpret_cast<const uint16_t*>(st + SW + SSB);
+            const uint4* xfr = reinterpret_cast<const uint4*>(st + SW + 2 * SSB);
+            const uint4* xbias = reinterpret_cast<const uint4*>(st + SW + 2 * SSB + XFB);
+            const float* xsig = reinterpret_cast<const float*>(st + SW + 2 * SSB + XFB + xprep_bias_bytes(MB));
+
+            // scales of this chunk for the two rows of each slab (8 binary16 each)
+            uint4 sv0[kSPW], sv1[kSPW];
+#pragma unroll
+            for (int sw = 0; sw < kSPW; ++sw) {
+                if (act[sw]) {
+                    sv0[sw] = *reinterpret_cast<const uint4*>(sst + row0[sw] * 8);
+                    sv1[sw] = *reinterpret_cast<const uint4*>(sst + (row0[sw] + 8) * 8);
+                } else {
+                    sv0[sw] = sv1[sw] = make_uint4(0, 0, 0, 0);
+                }
+            }
+
+#pragma unroll
+            for (int grp = 0; grp < kGPC; ++grp) {
+                if (grp < ng) {
+                    float P[kSPW][NT][4];
+#pragma unroll
+                    for (int sw = 0; sw < kSPW; ++sw)
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) P[sw][j][e] = 0.0f;
+#pragma unroll
+                    for (int v = 0; v < VB; ++v) {
+                        const int vb = grp * VB + v;
+                        uint4 bf[NT];
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) bf[j] = xfr[(vb * NT + j) * 32 + lane];
+#pragma unroll
+                        for (int sw = 0; sw < kSPW; ++sw) {
+                            if (act[sw]) {
+                                const uint32_t* blk0 = reinterpret_cast<const uint32_t*>(wst + row0[sw] * RS + vb * BB);
+                                const uint32_t* blk1 =
+                                    reinterpret_cast<const uint32_t*>(wst + (row0[sw] + 8) * RS + vb * BB);
+                                uint32_t ra[4], rb[4];
+                                unpack_block<BITS>(blk0, t, ra);
+                                unpack_block<BITS>(blk1, t, rb);
+#pragma unroll
+                                for (int j = 0; j < NT; ++j) {
+                                    mma_bf16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                    mma_bf16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int sw = 0; sw < kSPW; ++sw) {
+                        if (act[sw]) {
+                            const uint32_t w0 = (&sv0[sw].x)[grp >> 1];
+                            const uint32_t w1 = (&sv1[sw].x)[grp >> 1];
+                            const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(w0 >> (16 * (grp & 1)))));
+                            const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (grp & 1)))));
+#pragma unroll
+                            for (int j = 0; j < NT; ++j) {
+                                acc[sw][j][0] = fmaf(s0, P[sw][j][0], acc[sw][j][0]);
+                                acc[sw][j][1] = fmaf(s0, P[sw][j][1], acc[sw][j][1]);
+                                acc[sw][j][2] = fmaf(s1, P[sw][j][2], acc[sw][j][2]);
+                                acc[sw][j][3] = fmaf(s1, P[sw][j][3], acc[sw][j][3]);
+                            }
+                        }
+                    }
+                }
+            }
+
+            // bias and offset terms of the chunk: (b | s) x (XS | -OFF*XS) / sigma
+#pragma unroll
+            for (int sw = 0; sw < kSPW; ++sw) {
+                if (act[sw]) {
+                    uint32_t a0 = *reinterpret_cast<const uint32_t*>(bst + row0[sw] * 8 + 2 * t);
+                    uint32_t a1 = *reinterpret_cast<const uint32_t*>(bst + (row0[sw] + 8) * 8 + 2 * t);
+                    uint32_t a2 = *reinterpret_cast<const uint32_t*>(sst + row0[sw] * 8 + 2 * t);
+                    uint32_t a3 = *reinterpret_cast<const uint32_t*>(sst + (row0[sw] + 8) * 8 + 2 * t);
+                    if (ng < kGPC) {
+                        // groups past the end of K: stale shared memory, zero it
+                        const uint32_t keep = (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
+                        a0 &= keep;
+                        a1 &= keep;
+                        a2 &= keep;
+                        a3 &= keep;
+                    }
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const uint4 bb = xbias[j * 32 + lane];
+                        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        mma_f16(D, a0, a1, a2, a3, bb.x, bb.y);
+                        mma_f16(D, a0, a1, a2, a3, bb.z, bb.w);
+                        const float2 sg = *reinterpret_cast<const float2*>(xsig + 8 * j + 2 * t);
+                        acc[sw][j][0] = fmaf(sg.x, D[0], acc[sw][j][0]);
+                        acc[sw][j][1] = fmaf(sg.y, D[1], acc[sw][j][1]);
+                        acc[sw][j][2] = fmaf(sg.x, D[2], acc[sw][j][2]);
+                        acc[sw][j][3] = fmaf(sg.y, D[3], acc[sw][j][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            ++it;
+        }
+
+        // store: acc[sw][j][2h+e] is (row slab*16 + g + 8h, activation row 8j + 2t + e)
+        const BankPtrs bp = p.bank[bank];
+#pragma unroll
+        for (int sw = 0; sw < kSPW; ++sw) {
+            if (!act[sw]) continue;
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int nl = row0[sw] + 8 * h;
+                    if (nl >= rows) continue;
+                    const int64_t n = n0 + nl;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int m = 8 * j + 2 * t + e;
+                        if (m >= p.M) continue;
+                        const float v = acc[sw][j][2 * h + e];
+                        if (p.out_mode == kOutF32) {
+                            static_cast<float*>(bp.out)[m * p.N + n] = v;
+                        } else if (p.out_mode == kOutBF16) {
+                            static_cast<__nv_bfloat16*>(bp.out)[m * p.N + n] = __float2bfloat16_rn(v);
+                        } else {
+                            p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
+                        }
+                    }
+                }
+            }
+        }
+        return true;
+    });
+}
+
+// ---------------------------------------------------------------------------
+// 3. Split-K reduce: out = sum_{s=0..S-1} partial[s] in slice order.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kReduceThreads) qmm_splitk_reduce_kernel(const __grid_constant__ ReduceParams p);
+
+// ---------------------------------------------------------------------------
+// Diagnostic unpack: one thread per (row, virtual block, lane position t).
+// ---------------------------------------------------------------------------
+template <int BITS>
+__global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restrict__ w, int64_t K, int64_t N,
+                                                         uint8_t* __restrict__ codes) {
+    constexpr int BB = vblock_bytes(BITS);
+    const int64_t vbk = (BITS == 8) ? K / 16 : K / 32;          // virtual blocks per row
+    const int64_t total = N * vbk * 4;
+    const int64_t row_bytes = K * BITS / 8;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(idx & 3);
+        const int64_t rest = idx >> 2;
+        const int64_t vb = rest % vbk;
+        const int64_t n = rest / vbk;
+        const uint32_t* blk = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(w) + n * row_bytes + vb * BB);
+        uint32_t r[4];
+        unpack_block<BITS>(blk, t, r);
+        auto val = [](uint32_t reg, int hi) -> int {
+            const uint32_t h = (reg >> (16 * hi)) & 0xFFFFu;
+            return ((h & 0xFF80u) == 0x4300u) ? static_cast<int>(h & 0x7Fu) : -1;
+        };
+        uint8_t* out = codes + n * K;
+        if constexpr (BITS == 8) {
+            const int64_t kb = vb * 16 + 4 * t;
+            const int l0 = val(r[0], 0), l2 = val(r[0], 1), h0 = val(r[1], 0), h2 = val(r[1], 1);
+            const int l1 = val(r[2], 0), l3 = val(r[2], 1), h1 = val(r[3], 0), h3 = val(r[3], 1);
+            auto comb = [](int lo, int hi) -> uint8_t {
+                return (lo < 0 || hi < 0 || lo > 15 || hi > 15) ? 0xFF : static_cast<uint8_t>(lo + 16 * hi);
+            };
+            out[kb + 0] = comb(l0, h0);
+            out[kb + 1] = comb(l1, h1);
+            out[kb + 2] = comb(l2, h2);
+            out[kb + 3] = comb(l3, h3);
+        } else {
+            const int64_t kb = vb * 32 + 8 * t;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int lo = val(r[q], 0), hi = val(r[q], 1);
+                out[kb + q] = lo < 0 ? 0xFF : static_cast<uint8_t>(lo);
+                out[kb + q + 4] = hi < 0 ? 0xFF : static_cast<uint8_t>(hi);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch helpers (defined per code width in qmm_inst_b*.cu).
+// ---------------------------------------------------------------------------
+struct LaunchCfg {
+    const uint16_t* x;
+    int M;
+    int mb;            // 8 or 16
+    int ctas;
+    int smem;
+    cudaStream_t stream;
+};
+
+template <int BITS>
+cudaError_t configure_kernels(int group, int mb, int smem_bytes);
+template <int BITS>
+cudaError_t launch_forward(int group, const LaunchCfg& L, const MainParams& mp);
+template <int BITS>
+cudaError_t launch_unpack(const uint32_t* w, int64_t K, int64_t N, uint8_t* codes, cudaStream_t stream);
+
+cudaError_t launch_reduce(const ReduceParams& rp, int64_t elems, cudaStream_t stream);
+
+}  // namespace qmmk

@@ -1,0 +1,80 @@
+// Layout constants of the qmm kernels, shared by the host dispatch and the
+// device code (both sides of the library; nothing here is used by the oracle).
+//
+// Work decomposition (one main-kernel CTA per SM):
+//   * K is cut into chunks of kGPC = 8 scale groups; one pipeline stage holds
+//     one chunk for a row block of up to kTN = 128 weight rows: the packed
+//     code bytes of those rows, their 8 scales and 8 biases, and the staged
+//     activation fragments of the chunk.
+//   * A row block is 8 slabs of 16 rows; consumer warp w owns slabs w and
+//     w + kNCW (kNCW = 4 consumer warps), plus one producer warp.
+//   * Inside a slab the contraction runs on tensor cores with
+//     mma.m16n8k16: A = 16 weight rows x 16 codes (unpacked to bf16 128 + q),
+//     B = 16 codes x 8 activation rows, fp32 accumulators. One "virtual k32
+//     block" feeds two such MMAs. 8-bit codes are split into their two nibbles
+//     (weights 1 and 16), so an 8-bit k32 block of real codes is two virtual
+//     blocks.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define QMM_HD __host__ __device__ __forceinline__
+#else
+#define QMM_HD inline
+#endif
+
+namespace qmmk {
+
+constexpr int kGPC = 8;            // scale groups per chunk (pipeline stage)
+constexpr int kTN = 128;           // weight rows per row block
+constexpr int kSlab = 16;          // rows per MMA slab
+constexpr int kNCW = 4;            // consumer warps
+constexpr int kSPW = 2;            // slabs per consumer warp
+constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr int kXprepThreads = 256;
+constexpr int kReduceThreads = 256;
+
+QMM_HD constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Virtual k32 blocks per scale group (an 8-bit code counts as two nibbles).
+QMM_HD constexpr int vblocks_per_group(int bits, int group) {
+    return (group / 32) * (bits == 8 ? 2 : 1);
+}
+QMM_HD constexpr int vblocks_per_chunk(int bits, int group) {
+    return kGPC * vblocks_per_group(bits, group);
+}
+// Bytes of one weight row that one virtual block consumes.
+QMM_HD constexpr int vblock_bytes(int bits) { return bits == 8 ? 16 : 4 * bits; }
+// Packed bytes of one weight row in a full chunk, and its padded smem stride
+// (stride = 16 mod 32 bytes keeps the 8 row-groups of a warp on distinct banks).
+QMM_HD constexpr int chunk_row_bytes(int bits, int group) { return kGPC * group * bits / 8; }
+QMM_HD constexpr int chunk_row_stride(int bits, int group) { return chunk_row_bytes(bits, group) + 16; }
+
+// Staged activations, per chunk: MMA B fragments (one 16-byte vector per lane
+// per virtual block per 8-row tile), the bias-term fragments, and one scale
+// factor per activation row.
+QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
+QMM_HD constexpr int xprep_frag_bytes(int bits, int group, int mb) {
+    return vblocks_per_chunk(bits, group) * n8_tiles(mb) * 512;
+}
+QMM_HD constexpr int xprep_bias_bytes(int mb) { return n8_tiles(mb) * 512; }
+QMM_HD constexpr int xprep_chunk_bytes(int bits, int group, int mb) {
+    return round_up(xprep_frag_bytes(bits, group, mb) + xprep_bias_bytes(mb) + mb * 4, 128);
+}
+
+// One pipeline stage in shared memory.
+QMM_HD constexpr int stage_weight_bytes(int bits, int group) {
+    return round_up(kTN * chunk_row_stride(bits, group), 128);
+}
+QMM_HD constexpr int stage_sb_bytes() { return kTN * 16; }   // 8 binary16 values per row
+QMM_HD constexpr int stage_bytes(int bits, int group, int mb) {
+    return stage_weight_bytes(bits, group) + 2 * stage_sb_bytes() + xprep_chunk_bytes(bits, group, mb);
+}
+
+// Offset the unpacked codes carry (128 per bf16 slot; an 8-bit code is
+// 16*(128+hi) + (128+lo) over its two slots = q + 2176).
+QMM_HD constexpr float code_offset(int bits) { return bits == 8 ? 2176.0f : 128.0f; }
+
+}  // namespace qmmk
