@@ -411,6 +411,34 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_ncu_case(args):
+    """A small, untimed case for profilers: `calls` qmm_forward calls with M rows on
+    one weight copy of the workload (about 60 MB on the device)."""
+    import torch
+    from bit_affine_quantized_group_gb300 import _build
+    _build.build()
+    import bit_affine_quantized_group_gb300 as q
+    wl = datagen.WORKLOADS[args.case_workload]
+    bits = args.case_bits or wl["bits"][0]
+    K, N, group = wl["K"], wl["N"], wl["group"]
+    M = args.ncu_case
+    B = wl["banks"]
+    inp = datagen.gen_qmm(datagen.workload_seed(args.case_workload), M, K, N, bits, group, banks=B)
+    x = torch.from_numpy(inp.x.view(np.int16)).cuda().view(torch.bfloat16)
+    W = [torch.from_numpy(inp.words[i].view(np.int32)).cuda() for i in range(B)]
+    S = [torch.from_numpy(inp.scales[i].view(np.int16)).cuda().view(torch.float16) for i in range(B)]
+    Bi = [torch.from_numpy(inp.biases[i].view(np.int16)).cuda().view(torch.float16) for i in range(B)]
+    plan = q.Plan(K, N, bits, group, max_M=M, out_dtype=wl["out"], splits=args.case_splits, max_banks=B)
+    outs = [torch.empty((M, N), dtype=plan.out_dtype, device="cuda") for _ in range(B)]
+    for _ in range(args.calls):
+        if B == 1:
+            q.forward(plan, x, W[0], S[0], Bi[0], outs[0])
+        else:
+            q.forward_banked(plan, x, W, S, Bi, outs)
+    torch.cuda.synchronize()
+    print(f"ncu case ok: {args.case_workload} M={M} bits={bits} splits={plan.info()['splits']} calls={args.calls}")
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -418,7 +446,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA graph replay")
+    ap.add_argument("--ncu-case", type=int, default=0, metavar="M",
+                    help="run a small untimed profiling case with M rows and exit")
+    ap.add_argument("--case-workload", default=WORKLOAD, choices=sorted(datagen.WORKLOADS))
+    ap.add_argument("--case-bits", type=int, default=0)
+    ap.add_argument("--case-splits", type=int, default=0)
+    ap.add_argument("--calls", type=int, default=5)
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
     ws, rank, local = dist_env()
     if args.impl == "reference":
         run_reference(args, ws, rank)

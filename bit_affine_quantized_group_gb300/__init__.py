@@ -9,7 +9,8 @@ the library's CUDA kernels. PyTorch is used for device memory and streams.
     qmm.forward(plan, x, w, s, b, out)        # tensors on the plan's device
 
 The library is built by ``bit_affine_quantized_group_gb300._build`` (nvcc for
-sm_103a). There is no fallback: if the library is missing, import fails.
+sm_103a). There is no fallback: if the library is missing, the first call
+raises ImportError.
 """
 from __future__ import annotations
 
@@ -85,11 +86,25 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-lib = _load()
+_LIB = None
+
+
+def _lib() -> ctypes.CDLL:
+    """The loaded libqmm.so (loaded on first use; ImportError if it was never built)."""
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _lib()
+    raise AttributeError(name)
 
 
 def status_string(status: int) -> str:
-    return lib.qmm_status_string(int(status)).decode()
+    return _lib().qmm_status_string(int(status)).decode()
 
 
 def _out_code(out_dtype) -> int:
@@ -114,11 +129,11 @@ def make_desc(K, N, bits, group, max_M=16, out_dtype="bf16", splits=0, max_banks
 
 
 def validate_desc(desc: QmmDesc) -> int:
-    return int(lib.qmm_validate_desc(ctypes.byref(desc)))
+    return int(_lib().qmm_validate_desc(ctypes.byref(desc)))
 
 
 def workspace_bytes(desc: QmmDesc) -> int:
-    return int(lib.qmm_workspace_bytes(ctypes.byref(desc)))
+    return int(_lib().qmm_workspace_bytes(ctypes.byref(desc)))
 
 
 def _stream_handle(stream) -> int:
@@ -152,10 +167,10 @@ class Plan:
                 self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
                 base = self.workspace.data_ptr()
                 aligned = (base + 255) // 256 * 256
-                st = lib.qmm_plan(ctypes.byref(self._handle), ctypes.byref(self.desc), ctypes.c_void_p(aligned),
+                st = _lib().qmm_plan(ctypes.byref(self._handle), ctypes.byref(self.desc), ctypes.c_void_p(aligned),
                                   ctypes.c_size_t(nbytes))
             else:
-                st = lib.qmm_plan(ctypes.byref(self._handle), ctypes.byref(self.desc), None, ctypes.c_size_t(0))
+                st = _lib().qmm_plan(ctypes.byref(self._handle), ctypes.byref(self.desc), None, ctypes.c_size_t(0))
         if st != QMM_OK:
             raise QmmError(st, "qmm_plan")
         self.device = dev
@@ -166,7 +181,7 @@ class Plan:
 
     def info(self) -> dict:
         inf = QmmPlanInfo()
-        st = lib.qmm_plan_get_info(self._handle, ctypes.byref(inf))
+        st = _lib().qmm_plan_get_info(self._handle, ctypes.byref(inf))
         if st != QMM_OK:
             raise QmmError(st, "qmm_plan_get_info")
         return {"splits": inf.splits, "chunks": inf.chunks, "stages": list(inf.stages),
@@ -175,14 +190,14 @@ class Plan:
 
     def error_flags(self) -> int:
         v = ctypes.c_uint32(0)
-        st = lib.qmm_plan_error(self._handle, ctypes.byref(v))
+        st = _lib().qmm_plan_error(self._handle, ctypes.byref(v))
         if st not in (QMM_OK, QMM_ERR_TIMEOUT):
             raise QmmError(st, "qmm_plan_error")
         return int(v.value)
 
     def close(self):
         if self._handle is not None and self._handle.value:
-            lib.qmm_destroy(self._handle)
+            _lib().qmm_destroy(self._handle)
             self._handle = ctypes.c_void_p()
 
     def __del__(self):
@@ -199,7 +214,7 @@ def _ptr(t) -> int:
 def forward(plan: Plan, x, w, s, b, out, stream=None) -> None:
     """out[M, N] = qmm(x[M, K], w, s, b) via qmm_forward (asynchronous on `stream`)."""
     M = int(x.shape[0]) if x.dim() == 2 else 1
-    st = lib.qmm_forward(plan.handle, ctypes.c_void_p(_ptr(x)), M, ctypes.c_void_p(_ptr(w)),
+    st = _lib().qmm_forward(plan.handle, ctypes.c_void_p(_ptr(x)), M, ctypes.c_void_p(_ptr(w)),
                          ctypes.c_void_p(_ptr(s)), ctypes.c_void_p(_ptr(b)), plan.K, plan.N, plan.bits,
                          plan.group, ctypes.c_void_p(_ptr(out)), ctypes.c_void_p(_stream_handle(stream)))
     if st != QMM_OK:
@@ -217,7 +232,7 @@ def forward_banked(plan: Plan, x, ws, ss, bs, outs, stream=None) -> None:
     """One launch for len(ws) projections sharing x (qmm_forward_banked)."""
     n = len(ws)
     M = int(x.shape[0]) if x.dim() == 2 else 1
-    st = lib.qmm_forward_banked(plan.handle, ctypes.c_void_p(_ptr(x)), M, n, _ptr_array(ws), _ptr_array(ss),
+    st = _lib().qmm_forward_banked(plan.handle, ctypes.c_void_p(_ptr(x)), M, n, _ptr_array(ws), _ptr_array(ss),
                                 _ptr_array(bs), plan.K, plan.N, plan.bits, plan.group, _ptr_array(outs),
                                 ctypes.c_void_p(_stream_handle(stream)))
     if st != QMM_OK:
@@ -235,7 +250,7 @@ def check_forward_args(desc: QmmDesc, x_ptr: int, M: int, w_ptrs, s_ptrs, b_ptrs
             a[i] = p
         return a
     n = len(w_ptrs) if w_ptrs is not None else 1
-    return int(lib.qmm_check_forward_args(ctypes.byref(desc), ctypes.c_void_p(x_ptr), int(M), n, arr(w_ptrs),
+    return int(_lib().qmm_check_forward_args(ctypes.byref(desc), ctypes.c_void_p(x_ptr), int(M), n, arr(w_ptrs),
                                           arr(s_ptrs), arr(b_ptrs), int(K), int(N), int(bits), int(group),
                                           arr(out_ptrs)))
 
@@ -244,7 +259,7 @@ def unpack_codes(w, K: int, N: int, bits: int, stream=None):
     """Run the kernels' in-register unpacking on packed words; returns uint8 [N, K]."""
     import torch
     codes = torch.empty((N, K), dtype=torch.uint8, device=w.device)
-    st = lib.qmm_unpack_codes(ctypes.c_void_p(_ptr(w)), int(K), int(N), int(bits), ctypes.c_void_p(_ptr(codes)),
+    st = _lib().qmm_unpack_codes(ctypes.c_void_p(_ptr(w)), int(K), int(N), int(bits), ctypes.c_void_p(_ptr(codes)),
                               ctypes.c_void_p(_stream_handle(stream)))
     if st != QMM_OK:
         raise QmmError(st, "qmm_unpack_codes")

@@ -165,14 +165,14 @@ int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_by
     for (int i = 0; i < nmb; ++i) {
         const int mb = i == 0 ? 8 : 16;
         const int sb = stage_bytes(d->bits, d->group, mb);
-        int st = (optin - 1024) / (sb + 16);
+        int st = (optin - 1024 - reduce_scratch_bytes(mb)) / (sb + 16);
         if (st > kMaxStages) st = kMaxStages;
         if (st < 2) {
             delete p;
             return QMM_ERR_UNSUPPORTED;
         }
         p->stages[i] = st;
-        p->smem[i] = st * sb + st * 16;
+        p->smem[i] = main_smem_bytes(d->bits, d->group, mb, st);
         if (configure(d->bits, d->group, mb, p->smem[i]) != cudaSuccess) {
             delete p;
             return QMM_ERR_CUDA;
@@ -272,6 +272,7 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
     mp.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
     mp.sb_vec16 = (p->G % 8 == 0) ? 1 : 0;
     mp.banks = n_banks;
+    mp.xprep_bytes = static_cast<int64_t>(p->C) * xprep_chunk_bytes(bits, group, mi == 0 ? 8 : 16);
     mp.rows_total = static_cast<int64_t>(n_banks) * p->splits * N;
     for (int i = 0; i < n_banks; ++i) {
         mp.bank[i].w = packed_w[i];

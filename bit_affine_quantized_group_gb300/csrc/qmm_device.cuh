@@ -15,6 +15,18 @@ namespace qmmk {
 constexpr uint32_t kErrFullWait = 1u;     // consumer gave up waiting for a stage
 constexpr uint32_t kErrEmptyWait = 2u;    // producer gave up waiting for a free slot
 constexpr uint32_t kErrDrainWait = 4u;    // producer gave up draining its copies
+constexpr uint32_t kErrBadCopy = 8u;      // a copy failed its bounds/alignment check and was skipped
+
+// Record a rejected copy: error bit plus (first) offending address and size in
+// err[2..5]; the copy itself is skipped.
+__device__ __forceinline__ void record_bad_copy(uint32_t* err, const void* a, uint64_t b, uint32_t what) {
+    if (atomicOr(err, kErrBadCopy) & kErrBadCopy) return;
+    const uint64_t av = reinterpret_cast<uint64_t>(a);
+    err[2] = static_cast<uint32_t>(av);
+    err[3] = static_cast<uint32_t>(av >> 32);
+    err[4] = static_cast<uint32_t>(b);
+    err[5] = what;
+}
 
 // A pipeline wait that has not finished after this long is treated as a hang:
 // the kernel records it and returns instead of spinning forever.
@@ -99,12 +111,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 // Per-thread asynchronous copies (LDGSTS).
+// 16 bytes, L2-only, with an L2 eviction-priority policy (for streamed data).
+__device__ __forceinline__ void cp_async_16_hint(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 ::"r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
+}
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// Wait until all of this thread's cp.async copies have landed.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Arrive on `bar` once this thread's earlier cp.async copies have landed
 // (the arrival is pre-counted in the barrier's initial count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
@@ -119,6 +138,24 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D = A*B (zero accumulator), m16n8k16, A/B bf16.
+__device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+    const float z = 0.0f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+// D = A*B (zero accumulator), m16n8k16, A/B binary16.
+__device__ __forceinline__ void mma_f16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+    const float z = 0.0f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 // Same with binary16 operands.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

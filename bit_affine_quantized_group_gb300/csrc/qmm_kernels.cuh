@@ -8,8 +8,9 @@
 //                            commit) as split binary16 fragments, and one
 //                            power-of-two range factor per (row, chunk).
 //   2. qmm_main_kernel    -- one CTA per SM; a producer warp streams packed code
-//                            rows (1-D TMA bulk copies), scales and biases
-//                            (cp.async) and the staged activations into a ring of
+//                            rows, scales and biases (16-byte cp.async pieces)
+//                            and the staged activations (one TMA bulk copy per
+//                            chunk) into a ring of
 //                            shared-memory stages; four consumer warps unpack the
 //                            codes in registers and contract them on tensor cores,
 //                            reading each code byte once for all M rows (same
@@ -62,6 +63,7 @@ struct MainParams {
     int out_mode;
     int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
     int banks;
+    int64_t xprep_bytes;    // extent of the staged-activation region (for copy checks)
     BankPtrs bank[kMaxBanks];
 };
 
@@ -216,6 +218,10 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
 // ---------------------------------------------------------------------------
 // 2. Main kernel.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void consumer_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kNCW * 32) : "memory");
+}
+
 template <int BITS, int GROUP, int MB>
 __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_constant__ MainParams p) {
     constexpr int VB = vblocks_per_group(BITS, GROUP);
@@ -233,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     const int S = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
     uint64_t* empty = full + S;
+    float* scratch = reinterpret_cast<float*>(smem + S * SB + S * 16);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -248,6 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
 
     if (warp == kNCW) {
         // ------------------------------ producer ------------------------------
+        // Each lane owns a fixed (row offset, 16-byte piece) of every full chunk,
+        // so a copy costs one cp.async plus two pointer increments.
+        constexpr int PPR = RB / 16;                      // pieces per row, <= 32
+        constexpr int RPI = 32 / PPR;                     // rows per lane-sweep
+        const int lr = lane / PPR;
+        const int lq = lane - lr * PPR;
+        const bool lane_w = lr < RPI;
         const uint64_t pol = policy_evict_first();
         uint32_t it = 0;
         bool waited = false;
@@ -255,55 +269,90 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
         int npend = 0;
         int pend_slot[kMaxStages];
         int pend_chunk[kMaxStages];
+        auto issue_xprep = [&](int slot, int c) {
+            uint8_t* d = smem + slot * SB + SW + 2 * SSB;
+            const int64_t off = static_cast<int64_t>(c) * XPB;
+            if (slot < 0 || slot >= S || c < 0 || off + XPB > p.xprep_bytes ||
+                ((reinterpret_cast<uintptr_t>(p.xprep + off) | smem_u32(d)) & 15)) {
+                record_bad_copy(p.err, p.xprep + off, static_cast<uint64_t>(slot) << 32 | static_cast<uint32_t>(c), 3u);
+                return;
+            }
+            bulk_g2s(d, p.xprep + off, XPB, &full[slot]);
+        };
         auto flush_pending = [&]() {
             griddep_wait();   // the staged activations of this call are ready
             waited = true;
             if (lane == 0)
-                for (int i = 0; i < npend; ++i)
-                    bulk_g2s(smem + pend_slot[i] * SB + SW + 2 * SSB, p.xprep + static_cast<size_t>(pend_chunk[i]) * XPB,
-                             XPB, &full[pend_slot[i]]);
+                for (int i = 0; i < npend; ++i) issue_xprep(pend_slot[i], pend_chunk[i]);
             npend = 0;
         };
         for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
             (void)split;
             const BankPtrs bp = p.bank[bank];
+            // One check per row block that every copy below stays inside its buffers
+            // (rows n0..n0+rows-1, chunks c0..c1-1) and is 16-byte aligned; a failing
+            // block is recorded and its copies skipped.
+            const uint8_t* wrow0 = reinterpret_cast<const uint8_t*>(bp.w) + n0 * p.row_bytes;
+            const bool blk_ok =
+                n0 >= 0 && rows >= 1 && rows <= kTN && n0 + rows <= p.N && c0 >= 0 && c1 <= p.C &&
+                ((reinterpret_cast<uintptr_t>(wrow0) | static_cast<uintptr_t>(p.row_bytes)) & 15) == 0 &&
+                static_cast<int64_t>(c1) * RB <= p.row_bytes + RB &&
+                ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & (p.sb_vec16 ? 15 : 3)) == 0;
+            if (!blk_ok && lane == 0) record_bad_copy(p.err, wrow0, static_cast<uint64_t>(rows), 4u);
             for (int c = c0; c < c1; ++c) {
                 const int slot = static_cast<int>(it % S);
-                if (it >= static_cast<uint32_t>(S) &&
-                    !mbar_wait(&empty[slot], ((it / S) - 1) & 1u, p.err, kErrEmptyWait)) {
+                // After a timed-out wait the error is recorded and no further waits are
+                // made; the loop still runs to the end so that every warp finishes.
+                if (it >= static_cast<uint32_t>(S) && ok &&
+                    !mbar_wait(&empty[slot], ((it / S) - 1) & 1u, p.err, kErrEmptyWait))
                     ok = false;
-                    return false;
-                }
                 const int ng = min(kGPC, p.G - c * kGPC);
                 const uint32_t wbytes = static_cast<uint32_t>(ng * GROUP * BITS / 8);
                 uint8_t* st = smem + slot * SB;
-                if (lane == 0) mbar_arrive_expect_tx(&full[slot], rows * wbytes + XPB);
+                if (lane == 0) mbar_arrive_expect_tx(&full[slot], XPB);
                 __syncwarp();
-                const uint8_t* wsrc = reinterpret_cast<const uint8_t*>(bp.w) + n0 * p.row_bytes +
-                                      static_cast<int64_t>(c) * RB;
-                for (int r = lane; r < rows; r += 32)
-                    bulk_g2s_stream(st + r * RS, wsrc + r * p.row_bytes, wbytes, &full[slot], pol);
-                uint8_t* sdst = st + SW;
-                uint8_t* bdst = sdst + SSB;
-                const uint16_t* ssrc = bp.s + n0 * p.G + c * kGPC;
-                const uint16_t* bsrc = bp.b + n0 * p.G + c * kGPC;
-                if (p.sb_vec16) {
-                    for (int r = lane; r < rows; r += 32) {
-                        cp_async_16(sdst + r * 16, ssrc + static_cast<int64_t>(r) * p.G);
-                        cp_async_16(bdst + r * 16, bsrc + static_cast<int64_t>(r) * p.G);
+                const uint8_t* wsrc = wrow0 + static_cast<int64_t>(c) * RB;
+                if (blk_ok) {
+                    if (ng == kGPC) {
+                        if (lane_w) {
+                            uint8_t* d = st + lr * RS + 16 * lq;
+                            const uint8_t* g = wsrc + lr * p.row_bytes + 16 * lq;
+                            const int64_t gstep = RPI * p.row_bytes;
+#pragma unroll 4
+                            for (int r = lr; r < rows; r += RPI) {
+                                cp_async_16_hint(d, g, pol);
+                                d += RPI * RS;
+                                g += gstep;
+                            }
+                        }
+                    } else {
+                        const int pieces = static_cast<int>(wbytes >> 4);
+                        for (int i = lane; i < rows * pieces; i += 32) {
+                            const int r = i / pieces, q = i - (i / pieces) * pieces;
+                            cp_async_16_hint(st + r * RS + 16 * q, wsrc + r * p.row_bytes + 16 * q, pol);
+                        }
                     }
-                } else {
-                    const int nq = ng >> 1;   // 4-byte pieces per row
-                    for (int i = lane; i < rows * nq; i += 32) {
-                        const int r = i / nq, q = i - (i / nq) * nq;
-                        cp_async_4(sdst + r * 16 + 4 * q, ssrc + static_cast<int64_t>(r) * p.G + 2 * q);
-                        cp_async_4(bdst + r * 16 + 4 * q, bsrc + static_cast<int64_t>(r) * p.G + 2 * q);
+                    uint8_t* sdst = st + SW;
+                    uint8_t* bdst = sdst + SSB;
+                    const uint16_t* ssrc = bp.s + n0 * p.G + c * kGPC;
+                    const uint16_t* bsrc = bp.b + n0 * p.G + c * kGPC;
+                    if (p.sb_vec16) {
+                        for (int r = lane; r < rows; r += 32) {
+                            cp_async_16(sdst + r * 16, ssrc + static_cast<int64_t>(r) * p.G);
+                            cp_async_16(bdst + r * 16, bsrc + static_cast<int64_t>(r) * p.G);
+                        }
+                    } else {
+                        const int nq = ng >> 1;   // 4-byte pieces per row
+                        for (int i = lane; i < rows * nq; i += 32) {
+                            const int r = i / nq, q = i - (i / nq) * nq;
+                            cp_async_4(sdst + r * 16 + 4 * q, ssrc + static_cast<int64_t>(r) * p.G + 2 * q);
+                            cp_async_4(bdst + r * 16 + 4 * q, bsrc + static_cast<int64_t>(r) * p.G + 2 * q);
+                        }
                     }
                 }
                 cp_async_arrive_noinc(&full[slot]);
                 if (waited) {
-                    if (lane == 0)
-                        bulk_g2s(st + SW + 2 * SSB, p.xprep + static_cast<size_t>(c) * XPB, XPB, &full[slot]);
+                    if (lane == 0) issue_xprep(slot, c);
                 } else {
                     pend_slot[npend] = slot;
                     pend_chunk[npend] = c;
@@ -314,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
             return true;
         });
         if (!waited) flush_pending();
+        // This warp's own cp.async copies must land before it exits.
+        cp_async_wait_all();
         if (!ok) {
             // Give the copies already issued a bounded chance to land before exiting.
             const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0u;
@@ -326,14 +377,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     // -------------------------------- consumers --------------------------------
     const int g = lane >> 2;
     const int t = lane & 3;
+    const int sp = warp % kSlabPairs;        // slabs sp and sp + 4
+    const int kh = warp / kSlabPairs;        // chunk groups 4*kh .. 4*kh + 3
+    const int gbase = kh * kGroupsPerWarp;
     uint32_t it = 0;
+    bool ok = true;
     for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
         const int nsl = (rows + kSlab - 1) / kSlab;
         bool act[kSPW];
         int row0[kSPW];
 #pragma unroll
         for (int sw = 0; sw < kSPW; ++sw) {
-            const int slab = warp + sw * kNCW;
+            const int slab = sp + sw * kSlabPairs;
             act[sw] = slab < nsl;
             row0[sw] = slab * kSlab + g;
         }
@@ -347,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
 
         for (int c = c0; c < c1; ++c) {
             const int slot = static_cast<int>(it % S);
-            if (!mbar_wait(&full[slot], (it / S) & 1u, p.err, kErrFullWait)) return false;
+            // a timed-out wait is recorded; the warp then stops waiting but keeps the
+            // same control flow, so the consumer barriers below are always reached
+            if (ok && !mbar_wait(&full[slot], (it / S) & 1u, p.err, kErrFullWait)) ok = false;
             const int ng = min(kGPC, p.G - c * kGPC);
             const uint8_t* st = smem + slot * SB;
             const uint8_t* wst = st;
@@ -357,31 +414,21 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
             const uint4* xbias = reinterpret_cast<const uint4*>(st + SW + 2 * SSB + XFB);
             const float* xsig = reinterpret_cast<const float*>(st + SW + 2 * SSB + XFB + xprep_bias_bytes(MB));
 
-            // scales of this chunk for the two rows of each slab (8 binary16 each)
-            uint4 sv0[kSPW], sv1[kSPW];
+            // this warp's 4 scales for each of its slab rows (binary16 pairs)
+            uint2 sv0[kSPW], sv1[kSPW];
 #pragma unroll
             for (int sw = 0; sw < kSPW; ++sw) {
-                if (act[sw]) {
-                    sv0[sw] = *reinterpret_cast<const uint4*>(sst + row0[sw] * 8);
-                    sv1[sw] = *reinterpret_cast<const uint4*>(sst + (row0[sw] + 8) * 8);
-                } else {
-                    sv0[sw] = sv1[sw] = make_uint4(0, 0, 0, 0);
-                }
+                sv0[sw] = *reinterpret_cast<const uint2*>(sst + row0[sw] * 8 + gbase);
+                sv1[sw] = *reinterpret_cast<const uint2*>(sst + (row0[sw] + 8) * 8 + gbase);
             }
 
 #pragma unroll
-            for (int grp = 0; grp < kGPC; ++grp) {
-                if (grp < ng) {
+            for (int gl = 0; gl < kGroupsPerWarp; ++gl) {
+                if (gbase + gl < ng) {
                     float P[kSPW][NT][4];
 #pragma unroll
-                    for (int sw = 0; sw < kSPW; ++sw)
-#pragma unroll
-                        for (int j = 0; j < NT; ++j)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) P[sw][j][e] = 0.0f;
-#pragma unroll
                     for (int v = 0; v < VB; ++v) {
-                        const int vb = grp * VB + v;
+                        const int vb = (gbase + gl) * VB + v;
                         uint4 bf[NT];
 #pragma unroll
                         for (int j = 0; j < NT; ++j) bf[j] = xfr[(vb * NT + j) * 32 + lane];
@@ -396,7 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                                 unpack_block<BITS>(blk1, t, rb);
 #pragma unroll
                                 for (int j = 0; j < NT; ++j) {
-                                    mma_bf16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                    if (v == 0)
+                                        mma_bf16_zc(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                    else
+                                        mma_bf16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
                                     mma_bf16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
                                 }
                             }
@@ -405,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
 #pragma unroll
                     for (int sw = 0; sw < kSPW; ++sw) {
                         if (act[sw]) {
-                            const uint32_t w0 = (&sv0[sw].x)[grp >> 1];
-                            const uint32_t w1 = (&sv1[sw].x)[grp >> 1];
-                            const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(w0 >> (16 * (grp & 1)))));
-                            const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (grp & 1)))));
+                            const uint32_t w0 = (gl < 2) ? sv0[sw].x : sv0[sw].y;
+                            const uint32_t w1 = (gl < 2) ? sv1[sw].x : sv1[sw].y;
+                            const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(w0 >> (16 * (gl & 1)))));
+                            const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (gl & 1)))));
 #pragma unroll
                             for (int j = 0; j < NT; ++j) {
                                 acc[sw][j][0] = fmaf(s0, P[sw][j][0], acc[sw][j][0]);
@@ -421,33 +471,36 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                 }
             }
 
-            // bias and offset terms of the chunk: (b | s) x (XS | -OFF*XS) / sigma
+            // bias and offset terms of the chunk, (b | s) x (XS | -OFF*XS) / sigma,
+            // taken by the second K half (the first does the final combine)
+            if (kh == 1) {
 #pragma unroll
-            for (int sw = 0; sw < kSPW; ++sw) {
-                if (act[sw]) {
-                    uint32_t a0 = *reinterpret_cast<const uint32_t*>(bst + row0[sw] * 8 + 2 * t);
-                    uint32_t a1 = *reinterpret_cast<const uint32_t*>(bst + (row0[sw] + 8) * 8 + 2 * t);
-                    uint32_t a2 = *reinterpret_cast<const uint32_t*>(sst + row0[sw] * 8 + 2 * t);
-                    uint32_t a3 = *reinterpret_cast<const uint32_t*>(sst + (row0[sw] + 8) * 8 + 2 * t);
-                    if (ng < kGPC) {
-                        // groups past the end of K: stale shared memory, zero it
-                        const uint32_t keep = (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
-                        a0 &= keep;
-                        a1 &= keep;
-                        a2 &= keep;
-                        a3 &= keep;
-                    }
+                for (int sw = 0; sw < kSPW; ++sw) {
+                    if (act[sw]) {
+                        uint32_t a0 = *reinterpret_cast<const uint32_t*>(bst + row0[sw] * 8 + 2 * t);
+                        uint32_t a1 = *reinterpret_cast<const uint32_t*>(bst + (row0[sw] + 8) * 8 + 2 * t);
+                        uint32_t a2 = *reinterpret_cast<const uint32_t*>(sst + row0[sw] * 8 + 2 * t);
+                        uint32_t a3 = *reinterpret_cast<const uint32_t*>(sst + (row0[sw] + 8) * 8 + 2 * t);
+                        if (ng < kGPC) {
+                            // groups past the end of K: stale shared memory, zero it
+                            const uint32_t keep = (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
+                            a0 &= keep;
+                            a1 &= keep;
+                            a2 &= keep;
+                            a3 &= keep;
+                        }
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        const uint4 bb = xbias[j * 32 + lane];
-                        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                        mma_f16(D, a0, a1, a2, a3, bb.x, bb.y);
-                        mma_f16(D, a0, a1, a2, a3, bb.z, bb.w);
-                        const float2 sg = *reinterpret_cast<const float2*>(xsig + 8 * j + 2 * t);
-                        acc[sw][j][0] = fmaf(sg.x, D[0], acc[sw][j][0]);
-                        acc[sw][j][1] = fmaf(sg.y, D[1], acc[sw][j][1]);
-                        acc[sw][j][2] = fmaf(sg.x, D[2], acc[sw][j][2]);
-                        acc[sw][j][3] = fmaf(sg.y, D[3], acc[sw][j][3]);
+                        for (int j = 0; j < NT; ++j) {
+                            const uint4 bb = xbias[j * 32 + lane];
+                            float D[4];
+                            mma_f16_zc(D, a0, a1, a2, a3, bb.x, bb.y);
+                            mma_f16(D, a0, a1, a2, a3, bb.z, bb.w);
+                            const float2 sg = *reinterpret_cast<const float2*>(xsig + 8 * j + 2 * t);
+                            acc[sw][j][0] = fmaf(sg.x, D[0], acc[sw][j][0]);
+                            acc[sw][j][1] = fmaf(sg.y, D[1], acc[sw][j][1]);
+                            acc[sw][j][2] = fmaf(sg.x, D[2], acc[sw][j][2]);
+                            acc[sw][j][3] = fmaf(sg.y, D[3], acc[sw][j][3]);
+                        }
                     }
                 }
             }
@@ -456,36 +509,50 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
             ++it;
         }
 
-        // store: acc[sw][j][2h+e] is (row slab*16 + g + 8h, activation row 8j + 2t + e)
-        const BankPtrs bp = p.bank[bank];
+        // combine the two K halves in a fixed order: (first half) + (second half)
+        float* sc = scratch + ((sp * kSPW) * NT * 4) * 32;
+        if (kh == 1) {
 #pragma unroll
-        for (int sw = 0; sw < kSPW; ++sw) {
-            if (!act[sw]) continue;
+            for (int sw = 0; sw < kSPW; ++sw)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
+                for (int j = 0; j < NT; ++j)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int nl = row0[sw] + 8 * h;
-                    if (nl >= rows) continue;
-                    const int64_t n = n0 + nl;
+                    for (int e = 0; e < 4; ++e) sc[((sw * NT + j) * 4 + e) * 32 + lane] = acc[sw][j][e];
+        }
+        consumer_barrier();
+        if (kh == 0) {
+            const BankPtrs bp = p.bank[bank];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int m = 8 * j + 2 * t + e;
-                        if (m >= p.M) continue;
-                        const float v = acc[sw][j][2 * h + e];
-                        if (p.out_mode == kOutF32) {
-                            static_cast<float*>(bp.out)[m * p.N + n] = v;
-                        } else if (p.out_mode == kOutBF16) {
-                            static_cast<__nv_bfloat16*>(bp.out)[m * p.N + n] = __float2bfloat16_rn(v);
-                        } else {
-                            p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
+            for (int sw = 0; sw < kSPW; ++sw) {
+                if (!act[sw]) continue;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int nl = row0[sw] + 8 * h;
+                        if (nl >= rows) continue;
+                        const int64_t n = n0 + nl;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int m = 8 * j + 2 * t + e;
+                            if (m >= p.M) continue;
+                            const float v = acc[sw][j][2 * h + e] + sc[((sw * NT + j) * 4 + 2 * h + e) * 32 + lane];
+                            if (p.out_mode == kOutF32) {
+                                static_cast<float*>(bp.out)[m * p.N + n] = v;
+                            } else if (p.out_mode == kOutBF16) {
+                                static_cast<__nv_bfloat16*>(bp.out)[m * p.N + n] = __float2bfloat16_rn(v);
+                            } else {
+                                p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
+                            }
                         }
                     }
                 }
             }
         }
+        consumer_barrier();   // the scratch is free again
         return true;
     });
+    (void)ok;
 }
 
 // ---------------------------------------------------------------------------

@@ -6,8 +6,12 @@
 //     one chunk for a row block of up to kTN = 128 weight rows: the packed
 //     code bytes of those rows, their 8 scales and 8 biases, and the staged
 //     activation fragments of the chunk.
-//   * A row block is 8 slabs of 16 rows; consumer warp w owns slabs w and
-//     w + kNCW (kNCW = 4 consumer warps), plus one producer warp.
+//   * A row block is 8 slabs of 16 rows. There are 8 consumer warps and one
+//     producer warp. Consumer warp w owns slabs (w % 4) and (w % 4) + 4 and
+//     the groups 4*(w / 4) .. 4*(w / 4) + 3 of every chunk, so each slab pair
+//     is split between two warps along K; their partial sums are added in a
+//     fixed order through a small shared-memory scratch at the end of the row
+//     block.
 //   * Inside a slab the contraction runs on tensor cores with
 //     mma.m16n8k16: A = 16 weight rows x 16 codes (unpacked to bf16 128 + q),
 //     B = 16 codes x 8 activation rows, fp32 accumulators. One "virtual k32
@@ -29,8 +33,11 @@ namespace qmmk {
 constexpr int kGPC = 8;            // scale groups per chunk (pipeline stage)
 constexpr int kTN = 128;           // weight rows per row block
 constexpr int kSlab = 16;          // rows per MMA slab
-constexpr int kNCW = 4;            // consumer warps
+constexpr int kSlabPairs = 4;      // consumer warps along the rows
+constexpr int kKParts = 2;         // consumer warps along K (halves of a chunk)
+constexpr int kNCW = kSlabPairs * kKParts;   // consumer warps
 constexpr int kSPW = 2;            // slabs per consumer warp
+constexpr int kGroupsPerWarp = kGPC / kKParts;
 constexpr int kThreads = (kNCW + 1) * 32;
 constexpr int kMaxStages = 8;
 constexpr int kXprepThreads = 256;
@@ -71,6 +78,13 @@ QMM_HD constexpr int stage_weight_bytes(int bits, int group) {
 QMM_HD constexpr int stage_sb_bytes() { return kTN * 16; }   // 8 binary16 values per row
 QMM_HD constexpr int stage_bytes(int bits, int group, int mb) {
     return stage_weight_bytes(bits, group) + 2 * stage_sb_bytes() + xprep_chunk_bytes(bits, group, mb);
+}
+
+// Scratch for adding the two K halves of every slab pair at a row block's end.
+QMM_HD constexpr int reduce_scratch_bytes(int mb) { return kSlabPairs * kSPW * n8_tiles(mb) * 4 * 32 * 4; }
+// Dynamic shared memory of the main kernel with `stages` pipeline stages.
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int stages) {
+    return stages * stage_bytes(bits, group, mb) + stages * 16 + reduce_scratch_bytes(mb);
 }
 
 // Offset the unpacked codes carry (128 per bf16 slot; an 8-bit code is

@@ -148,7 +148,7 @@ def test_plan_mismatch_rejected(q):
 @pytest.mark.parametrize("splits", [1, 2, 3, 4, 8])
 def test_deterministic(q, splits):
     import torch
-    K, N, bits, group = 64 * 48, 1000, 4, 64
+    K, N, bits, group = 64 * 96, 1000, 4, 64   # 12 chunks: room for 8 slices
     inp = datagen.gen_qmm(99, 16, K, N, bits, group)
     plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="bf16", splits=splits)
     x, w, s, b = dev_tensors(inp)
