@@ -2,9 +2,13 @@
 // dispatch. Declarations and the contract are in include/qmm.h.
 #include <cuda_runtime.h>
 
+#include <cudaTypedefs.h>
+
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <unordered_map>
 
 #include "../../include/qmm.h"
 #include "qmm_kernels.cuh"
@@ -28,6 +32,8 @@ struct qmm_plan {
     uint32_t* err;       // device error word (start of the workspace)
     uint8_t* xprep;
     float* partial;
+    // TMA tensor maps already encoded for a given base pointer (weights, scales, biases)
+    std::unordered_map<const void*, CUtensorMap> wmaps, smaps, bmaps;
 };
 
 namespace {
@@ -84,14 +90,75 @@ cudaError_t configure(int bits, int group, int mb, int smem) {
     }
 }
 
-cudaError_t launch(int bits, int group, const LaunchCfg& L, const MainParams& mp) {
+cudaError_t launch(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,
+                   const MainParams<kMaxBanks>* banked) {
     switch (bits) {
-        case 4: return launch_forward<4>(group, L, mp);
-        case 5: return launch_forward<5>(group, L, mp);
-        case 6: return launch_forward<6>(group, L, mp);
-        case 8: return launch_forward<8>(group, L, mp);
+        case 4: return launch_forward<4>(group, L, single, banked);
+        case 5: return launch_forward<5>(group, L, single, banked);
+        case 6: return launch_forward<6>(group, L, single, banked);
+        case 8: return launch_forward<8>(group, L, single, banked);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Packed codes as uint8 [N][row_bytes]; box kTN rows x W bytes with the W-byte swizzle.
+bool encode_weights(const struct qmm_plan* p, const void* w, CUtensorMap* out) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const int W = weight_box_width(p->d.bits, p->d.group);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->d.K * p->d.bits / 8), static_cast<cuuint64_t>(p->d.N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->d.K * p->d.bits / 8)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(W), static_cast<cuuint32_t>(kTN)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = W == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                           : (W == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Scales or biases as uint16 [N][G]; box kTN rows x 8 values, unswizzled.
+bool encode_sb(const struct qmm_plan* p, const void* a, CUtensorMap* out) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->G), static_cast<cuuint64_t>(p->d.N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->G) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGPC), static_cast<cuuint32_t>(kTN)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Cached lookup; the cache is cleared when it grows past a few thousand pointers.
+bool tensor_map_for(struct qmm_plan* p, std::unordered_map<const void*, CUtensorMap>& cache, const void* ptr, bool weights,
+                    CUtensorMap* out) {
+    auto it = cache.find(ptr);
+    if (it != cache.end()) {
+        *out = it->second;
+        return true;
+    }
+    CUtensorMap m;
+    if (!(weights ? encode_weights(p, ptr, &m) : encode_sb(p, ptr, &m))) return false;
+    if (cache.size() >= 4096) cache.clear();
+    cache.emplace(ptr, m);
+    *out = m;
+    return true;
 }
 
 }  // namespace
@@ -165,7 +232,7 @@ int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_by
     for (int i = 0; i < nmb; ++i) {
         const int mb = i == 0 ? 8 : 16;
         const int sb = stage_bytes(d->bits, d->group, mb);
-        int st = (optin - 1024 - reduce_scratch_bytes(mb)) / (sb + 16);
+        int st = (optin - 2048 - reduce_scratch_bytes(mb)) / (sb + 16);
         if (st > kMaxStages) st = kMaxStages;
         if (st < 2) {
             delete p;
@@ -255,34 +322,30 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
     const int mi = mb_index(M);
     if (p->stages[mi] == 0) return QMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    struct qmm_plan* mp_plan = const_cast<struct qmm_plan*>(p);   // the tensor-map caches are plan-owned scratch
 
-    MainParams mp;
-    std::memset(&mp, 0, sizeof(mp));
-    mp.xprep = p->xprep;
-    mp.partial = p->partial;
-    mp.err = p->err;
-    mp.N = N;
-    mp.K = K;
-    mp.row_bytes = K * bits / 8;
-    mp.G = p->G;
-    mp.C = p->C;
-    mp.splits = p->splits;
-    mp.M = M;
-    mp.stages = p->stages[mi];
-    mp.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
-    mp.sb_vec16 = (p->G % 8 == 0) ? 1 : 0;
-    mp.banks = n_banks;
-    mp.xprep_bytes = static_cast<int64_t>(p->C) * xprep_chunk_bytes(bits, group, mi == 0 ? 8 : 16);
-    mp.rows_total = static_cast<int64_t>(n_banks) * p->splits * N;
-    for (int i = 0; i < n_banks; ++i) {
-        mp.bank[i].w = packed_w[i];
-        mp.bank[i].s = scales_f16[i];
-        mp.bank[i].b = biases_f16[i];
-        mp.bank[i].out = out[i];
-    }
-    int64_t ctas = (mp.rows_total + kSlab - 1) / kSlab;
+    MainHeader h;
+    std::memset(&h, 0, sizeof(h));
+    h.xprep = p->xprep;
+    h.partial = p->partial;
+    h.err = p->err;
+    h.N = N;
+    h.K = K;
+    h.row_bytes = K * bits / 8;
+    h.G = p->G;
+    h.C = p->C;
+    h.splits = p->splits;
+    h.M = M;
+    h.stages = p->stages[mi];
+    h.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
+    h.sb_tma = (p->G % 8 == 0) ? 1 : 0;
+    h.sb_vec16 = h.sb_tma;
+    h.banks = n_banks;
+    h.xprep_bytes = static_cast<int64_t>(p->C) * xprep_chunk_bytes(bits, group, mi == 0 ? 8 : 16);
+    h.rows_total = static_cast<int64_t>(n_banks) * p->splits * N;
+
+    int64_t ctas = (h.rows_total + kSlab - 1) / kSlab;
     if (ctas > p->num_sms) ctas = p->num_sms;
-
     LaunchCfg L;
     L.x = static_cast<const uint16_t*>(x_bf16);
     L.M = M;
@@ -290,7 +353,35 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
     L.ctas = static_cast<int>(ctas);
     L.smem = p->smem[mi];
     L.stream = st;
-    if (launch(bits, group, L, mp) != cudaSuccess) return QMM_ERR_CUDA;
+
+    auto fill = [&](auto& mp) -> bool {
+        mp.h = h;
+        for (int i = 0; i < n_banks; ++i) {
+            mp.bank[i].w = packed_w[i];
+            mp.bank[i].s = scales_f16[i];
+            mp.bank[i].b = biases_f16[i];
+            mp.bank[i].out = out[i];
+            if (!tensor_map_for(mp_plan, mp_plan->wmaps, packed_w[i], true, &mp.tmw[i])) return false;
+            if (h.sb_tma) {
+                if (!tensor_map_for(mp_plan, mp_plan->smaps, scales_f16[i], false, &mp.tms[i])) return false;
+                if (!tensor_map_for(mp_plan, mp_plan->bmaps, biases_f16[i], false, &mp.tmb[i])) return false;
+            }
+        }
+        return true;
+    };
+    cudaError_t le;
+    if (n_banks == 1) {
+        MainParams<1> mp1;
+        std::memset(&mp1, 0, sizeof(mp1));
+        if (!fill(mp1)) return QMM_ERR_CUDA;
+        le = launch(bits, group, L, &mp1, nullptr);
+    } else {
+        static thread_local MainParams<kMaxBanks> mpb;   // 25 KB: kept off the stack
+        std::memset(&mpb, 0, sizeof(mpb));
+        if (!fill(mpb)) return QMM_ERR_CUDA;
+        le = launch(bits, group, L, nullptr, &mpb);
+    }
+    if (le != cudaSuccess) return QMM_ERR_CUDA;
 
     if (p->splits > 1) {
         ReduceParams rp;

@@ -9,24 +9,25 @@ namespace qmmk {
 namespace {
 template <int BITS, int GROUP, int MB>
 cudaError_t configure_one(int smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB>,
+    cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    return cudaSuccess;
+    return cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, kMaxBanks>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-template <int BITS, int GROUP, int MB>
-cudaError_t launch_one(const LaunchCfg& L, const MainParams& mp) {
+template <int BITS, int GROUP, int MB, int CAP>
+cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     // (1) activation staging: ordinary stream order after the caller's work.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(mp.C));
+    cfg.gridDim = dim3(static_cast<unsigned>(mp.h.C));
     cfg.blockDim = dim3(kXprepThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = L.stream;
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_xprep_kernel<BITS, GROUP, MB>, L.x, L.M, mp.K, mp.G,
-                                       const_cast<uint8_t*>(mp.xprep));
+    cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_xprep_kernel<BITS, GROUP, MB>, L.x, L.M, mp.h.K, mp.h.G,
+                                       const_cast<uint8_t*>(mp.h.xprep));
     if (e != cudaSuccess) return e;
     // (2) main kernel as a programmatic dependent of (1).
     cudaLaunchAttribute attr[1];
@@ -37,7 +38,12 @@ cudaError_t launch_one(const LaunchCfg& L, const MainParams& mp) {
     cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB>, mp);
+    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP>, mp);
+}
+
+template <int BITS, int GROUP, int MB>
+cudaError_t launch_cap(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked) {
+    return single ? launch_one<BITS, GROUP, MB, 1>(L, *single) : launch_one<BITS, GROUP, MB, kMaxBanks>(L, *banked);
 }
 }  // namespace
 
@@ -50,10 +56,13 @@ cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, int smem_bytes) 
 }
 
 template <>
-cudaError_t launch_forward<QMM_INST_BITS>(int group, const LaunchCfg& L, const MainParams& mp) {
+cudaError_t launch_forward<QMM_INST_BITS>(int group, const LaunchCfg& L, const MainParams<1>* single,
+                                          const MainParams<kMaxBanks>* banked) {
     constexpr int B = QMM_INST_BITS;
-    if (group == 32) return L.mb == 8 ? launch_one<B, 32, 8>(L, mp) : launch_one<B, 32, 16>(L, mp);
-    if (group == 64) return L.mb == 8 ? launch_one<B, 64, 8>(L, mp) : launch_one<B, 64, 16>(L, mp);
+    if (group == 32)
+        return L.mb == 8 ? launch_cap<B, 32, 8>(L, single, banked) : launch_cap<B, 32, 16>(L, single, banked);
+    if (group == 64)
+        return L.mb == 8 ? launch_cap<B, 64, 8>(L, single, banked) : launch_cap<B, 64, 16>(L, single, banked);
     return cudaErrorInvalidValue;
 }
 

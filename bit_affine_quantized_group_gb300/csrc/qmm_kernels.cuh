@@ -32,6 +32,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "qmm_device.cuh"
 
 namespace qmmk {
@@ -47,7 +49,9 @@ struct BankPtrs {
 
 enum OutMode : int { kOutF32 = 0, kOutBF16 = 1, kOutPartial = 2 };
 
-struct MainParams {
+// Kernel parameters. CAP = number of bank slots carried (1 for a single
+// projection, kMaxBanks for banked calls), so single calls pass a small block.
+struct MainHeader {
     const uint8_t* xprep;   // per chunk: xprep_chunk_bytes(bits, group, MB)
     float* partial;         // [banks][splits][M][N] when out_mode == kOutPartial
     uint32_t* err;          // device error word
@@ -55,16 +59,25 @@ struct MainParams {
     int64_t K;
     int64_t row_bytes;      // K*bits/8
     int64_t rows_total;     // banks * splits * N
+    int64_t xprep_bytes;    // extent of the staged-activation region (for copy checks)
     int G;                  // K / group
     int C;                  // chunks = ceil(G / 8)
     int splits;
     int M;
     int stages;
     int out_mode;
+    int sb_tma;             // scales/biases by TMA boxes (G % 8 == 0), else cp.async
     int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
     int banks;
-    int64_t xprep_bytes;    // extent of the staged-activation region (for copy checks)
-    BankPtrs bank[kMaxBanks];
+};
+
+template <int CAP>
+struct MainParams {
+    MainHeader h;
+    BankPtrs bank[CAP];
+    CUtensorMap tmw[CAP];   // packed codes: uint8 [N][row_bytes], box kTN x W, swizzled
+    CUtensorMap tms[CAP];   // scales: uint16 [N][G], box kTN x 8 (when sb_tma)
+    CUtensorMap tmb[CAP];   // biases: same
 };
 
 struct ReduceParams {
@@ -83,7 +96,7 @@ struct ReduceParams {
 // (bank, split) boundaries and then into balanced row blocks of <= kTN rows.
 // ---------------------------------------------------------------------------
 template <typename F>
-__device__ __forceinline__ void for_each_row_block(const MainParams& p, F&& f) {
+__device__ __forceinline__ void for_each_row_block(const MainHeader& p, F&& f) {
     const int64_t r_begin = p.rows_total * blockIdx.x / gridDim.x;
     const int64_t r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
     int64_t r = r_begin;
@@ -222,20 +235,36 @@ __device__ __forceinline__ void consumer_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(kNCW * 32) : "memory");
 }
 
-template <int BITS, int GROUP, int MB>
-__global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_constant__ MainParams p) {
+// Byte offset, inside a stage, of byte b of weight-tile row r (TMA box layout
+// with the W-byte swizzle: 16-byte chunk bits 4.. of the in-box address are
+// XORed with its bits 7..).
+template <int BITS, int GROUP>
+__device__ __forceinline__ int wtile_off(int r, int b) {
+    constexpr int W = wbox_width(BITS, GROUP);
+    constexpr int LW = log2i(W);
+    constexpr int MASK = W / 16 - 1;
+    const int lin = r * W + (b & (W - 1));
+    return ((b >> LW) << (LW + 7)) + (lin ^ (((lin >> 7) & MASK) << 4));
+}
+
+template <int BITS, int GROUP, int MB, int CAP>
+__global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
     constexpr int VB = vblocks_per_group(BITS, GROUP);
     constexpr int NT = n8_tiles(MB);
     constexpr int BB = vblock_bytes(BITS);
-    constexpr int RS = chunk_row_stride(BITS, GROUP);
     constexpr int RB = chunk_row_bytes(BITS, GROUP);
+    constexpr int W = wbox_width(BITS, GROUP);
+    constexpr int NBOX = wbox_count(BITS, GROUP);
     constexpr int SW = stage_weight_bytes(BITS, GROUP);
     constexpr int SSB = stage_sb_bytes();
     constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
     constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
     constexpr int SB = stage_bytes(BITS, GROUP, MB);
+    constexpr int NV = kGroupsPerWarp * VB;        // virtual blocks per consumer warp per stage
+    const MainHeader& p = P.h;
 
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
     uint64_t* empty = full + S;
@@ -255,14 +284,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
 
     if (warp == kNCW) {
         // ------------------------------ producer ------------------------------
-        // Each lane owns a fixed (row offset, 16-byte piece) of every full chunk,
-        // so a copy costs one cp.async plus two pointer increments.
-        constexpr int PPR = RB / 16;                      // pieces per row, <= 32
-        constexpr int RPI = 32 / PPR;                     // rows per lane-sweep
-        const int lr = lane / PPR;
-        const int lq = lane - lr * PPR;
-        const bool lane_w = lr < RPI;
+        // Lane 0 issues the TMA boxes of a stage (packed codes, scales, biases)
+        // and the bulk copy of its staged activations. Scales and biases whose
+        // rows are not 16-byte multiples go through per-lane cp.async instead.
         const uint64_t pol = policy_evict_first();
+        if (lane == 0)
+            for (int i = 0; i < p.banks && i < CAP; ++i) {
+                prefetch_tensormap(&P.tmw[i]);
+                if (p.sb_tma) {
+                    prefetch_tensormap(&P.tms[i]);
+                    prefetch_tensormap(&P.tmb[i]);
+                }
+            }
+        const uint32_t tx_stage =
+            static_cast<uint32_t>(NBOX * kTN * W + (p.sb_tma ? 2 * SSB : 0) + XPB);
         uint32_t it = 0;
         bool waited = false;
         bool ok = true;
@@ -288,17 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
         };
         for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
             (void)split;
-            const BankPtrs bp = p.bank[bank];
-            // One check per row block that every copy below stays inside its buffers
-            // (rows n0..n0+rows-1, chunks c0..c1-1) and is 16-byte aligned; a failing
-            // block is recorded and its copies skipped.
-            const uint8_t* wrow0 = reinterpret_cast<const uint8_t*>(bp.w) + n0 * p.row_bytes;
-            const bool blk_ok =
-                n0 >= 0 && rows >= 1 && rows <= kTN && n0 + rows <= p.N && c0 >= 0 && c1 <= p.C &&
-                ((reinterpret_cast<uintptr_t>(wrow0) | static_cast<uintptr_t>(p.row_bytes)) & 15) == 0 &&
-                static_cast<int64_t>(c1) * RB <= p.row_bytes + RB &&
-                ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & (p.sb_vec16 ? 15 : 3)) == 0;
-            if (!blk_ok && lane == 0) record_bad_copy(p.err, wrow0, static_cast<uint64_t>(rows), 4u);
+            const BankPtrs bp = P.bank[bank];
+            // the cp.async path for scales/biases checks its buffers once per row block
+            const bool sb_ok = p.sb_tma ||
+                (n0 >= 0 && rows >= 1 && rows <= kTN && n0 + rows <= p.N && c0 >= 0 && c1 <= p.C &&
+                 ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & 3) == 0);
+            if (!sb_ok && lane == 0) record_bad_copy(p.err, bp.s, static_cast<uint64_t>(rows), 4u);
             for (int c = c0; c < c1; ++c) {
                 const int slot = static_cast<int>(it % S);
                 // After a timed-out wait the error is recorded and no further waits are
@@ -306,48 +336,30 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                 if (it >= static_cast<uint32_t>(S) && ok &&
                     !mbar_wait(&empty[slot], ((it / S) - 1) & 1u, p.err, kErrEmptyWait))
                     ok = false;
-                const int ng = min(kGPC, p.G - c * kGPC);
-                const uint32_t wbytes = static_cast<uint32_t>(ng * GROUP * BITS / 8);
                 uint8_t* st = smem + slot * SB;
-                if (lane == 0) mbar_arrive_expect_tx(&full[slot], XPB);
-                __syncwarp();
-                const uint8_t* wsrc = wrow0 + static_cast<int64_t>(c) * RB;
-                if (blk_ok) {
-                    if (ng == kGPC) {
-                        if (lane_w) {
-                            uint8_t* d = st + lr * RS + 16 * lq;
-                            const uint8_t* g = wsrc + lr * p.row_bytes + 16 * lq;
-                            const int64_t gstep = RPI * p.row_bytes;
-#pragma unroll 4
-                            for (int r = lr; r < rows; r += RPI) {
-                                cp_async_16_hint(d, g, pol);
-                                d += RPI * RS;
-                                g += gstep;
-                            }
-                        }
-                    } else {
-                        const int pieces = static_cast<int>(wbytes >> 4);
-                        for (int i = lane; i < rows * pieces; i += 32) {
-                            const int r = i / pieces, q = i - (i / pieces) * pieces;
-                            cp_async_16_hint(st + r * RS + 16 * q, wsrc + r * p.row_bytes + 16 * q, pol);
-                        }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], tx_stage);
+                    const int y = static_cast<int>(n0);
+#pragma unroll
+                    for (int bi = 0; bi < NBOX; ++bi)
+                        tma_load_2d(st + bi * (kTN * W), &P.tmw[bank], c * RB + bi * W, y, &full[slot], pol);
+                    if (p.sb_tma) {
+                        tma_load_2d(st + SW, &P.tms[bank], c * kGPC, y, &full[slot], pol);
+                        tma_load_2d(st + SW + SSB, &P.tmb[bank], c * kGPC, y, &full[slot], pol);
                     }
+                }
+                __syncwarp();
+                if (!p.sb_tma && sb_ok) {
+                    const int ng = min(kGPC, p.G - c * kGPC);
+                    const int nq = ng >> 1;   // 4-byte pieces per row
                     uint8_t* sdst = st + SW;
                     uint8_t* bdst = sdst + SSB;
                     const uint16_t* ssrc = bp.s + n0 * p.G + c * kGPC;
                     const uint16_t* bsrc = bp.b + n0 * p.G + c * kGPC;
-                    if (p.sb_vec16) {
-                        for (int r = lane; r < rows; r += 32) {
-                            cp_async_16(sdst + r * 16, ssrc + static_cast<int64_t>(r) * p.G);
-                            cp_async_16(bdst + r * 16, bsrc + static_cast<int64_t>(r) * p.G);
-                        }
-                    } else {
-                        const int nq = ng >> 1;   // 4-byte pieces per row
-                        for (int i = lane; i < rows * nq; i += 32) {
-                            const int r = i / nq, q = i - (i / nq) * nq;
-                            cp_async_4(sdst + r * 16 + 4 * q, ssrc + static_cast<int64_t>(r) * p.G + 2 * q);
-                            cp_async_4(bdst + r * 16 + 4 * q, bsrc + static_cast<int64_t>(r) * p.G + 2 * q);
-                        }
+                    for (int i = lane; i < rows * nq; i += 32) {
+                        const int r = i / nq, q = i - (i / nq) * nq;
+                        cp_async_4(sdst + r * 16 + 4 * q, ssrc + static_cast<int64_t>(r) * p.G + 2 * q);
+                        cp_async_4(bdst + r * 16 + 4 * q, bsrc + static_cast<int64_t>(r) * p.G + 2 * q);
                     }
                 }
                 cp_async_arrive_noinc(&full[slot]);
@@ -380,6 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     const int sp = warp % kSlabPairs;        // slabs sp and sp + 4
     const int kh = warp / kSlabPairs;        // chunk groups 4*kh .. 4*kh + 3
     const int gbase = kh * kGroupsPerWarp;
+    const int vbw = gbase * VB;              // first virtual block of this warp in a chunk
+    // Offsets of this lane's word in each of the warp's virtual blocks, for a
+    // tile row r with r % 8 == 0 (add r * W): box base + swizzled 16-byte chunk.
+    // Valid for the 4-bit and 8-bit layouts (128-byte boxes, one word per block).
+    int cx[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        if constexpr (BITS == 4 || BITS == 8)
+            cx[i] = (((vbw + i) >> 3) << 14) + (((((vbw + i) & 7) ^ g) << 4) | (4 * t));
+        else
+            cx[i] = 0;
+    }
     uint32_t it = 0;
     bool ok = true;
     for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
@@ -422,86 +446,101 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                 sv1[sw] = *reinterpret_cast<const uint2*>(sst + (row0[sw] + 8) * 8 + gbase);
             }
 
+            // The group loop, instantiated twice: without any guard for the common
+            // case (full chunk, both slabs live) so loads of later groups can be
+            // scheduled under the tensor-core work of earlier ones, and guarded for
+            // partial chunks and partial row blocks.
+            auto groups = [&](auto full_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
-            for (int gl = 0; gl < kGroupsPerWarp; ++gl) {
-                if (gbase + gl < ng) {
+                for (int gl = 0; gl < kGroupsPerWarp; ++gl) {
+                    if (!FULL && gbase + gl >= ng) continue;
                     float P[kSPW][NT][4];
 #pragma unroll
                     for (int v = 0; v < VB; ++v) {
-                        const int vb = (gbase + gl) * VB + v;
+                        const int vi = gl * VB + v;          // block index within the warp
+                        const int vb = vbw + vi;             // block index within the chunk
                         uint4 bf[NT];
 #pragma unroll
                         for (int j = 0; j < NT; ++j) bf[j] = xfr[(vb * NT + j) * 32 + lane];
 #pragma unroll
                         for (int sw = 0; sw < kSPW; ++sw) {
-                            if (act[sw]) {
-                                const uint32_t* blk0 = reinterpret_cast<const uint32_t*>(wst + row0[sw] * RS + vb * BB);
-                                const uint32_t* blk1 =
-                                    reinterpret_cast<const uint32_t*>(wst + (row0[sw] + 8) * RS + vb * BB);
-                                uint32_t ra[4], rb[4];
-                                unpack_block<BITS>(blk0, t, ra);
-                                unpack_block<BITS>(blk1, t, rb);
+                            if (!FULL && !act[sw]) continue;
+                            uint32_t ra[4], rb[4];
+                            if constexpr (BITS == 4 || BITS == 8) {
+                                const uint8_t* a0 = wst + (row0[sw] - g) * W + cx[vi];
+                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + g * W), ra);
+                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + (g + 8) * W), rb);
+                            } else {
+                                const int b0 = vb * BB + 4 * odd_word<BITS>(t);
+                                const int r0 = row0[sw], r1 = row0[sw] + 8;
+                                const uint32_t lo0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r0, b0));
+                                const uint32_t hi0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r0, b0 + 4));
+                                const uint32_t lo1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r1, b0));
+                                const uint32_t hi1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r1, b0 + 4));
+                                unpack_odd<BITS>(lo0, hi0, odd_shift<BITS>(t), ra);
+                                unpack_odd<BITS>(lo1, hi1, odd_shift<BITS>(t), rb);
+                            }
 #pragma unroll
-                                for (int j = 0; j < NT; ++j) {
-                                    if (v == 0)
-                                        mma_bf16_zc(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
-                                    else
-                                        mma_bf16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
-                                    mma_bf16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
-                                }
+                            for (int j = 0; j < NT; ++j) {
+                                if (v == 0)
+                                    mma_bf16_zc(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                else
+                                    mma_bf16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                mma_bf16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
                             }
                         }
                     }
 #pragma unroll
                     for (int sw = 0; sw < kSPW; ++sw) {
-                        if (act[sw]) {
-                            const uint32_t w0 = (gl < 2) ? sv0[sw].x : sv0[sw].y;
-                            const uint32_t w1 = (gl < 2) ? sv1[sw].x : sv1[sw].y;
-                            const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(w0 >> (16 * (gl & 1)))));
-                            const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (gl & 1)))));
+                        if (!FULL && !act[sw]) continue;
+                        const uint32_t w0 = (gl < 2) ? sv0[sw].x : sv0[sw].y;
+                        const uint32_t w1 = (gl < 2) ? sv1[sw].x : sv1[sw].y;
+                        const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(w0 >> (16 * (gl & 1)))));
+                        const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (gl & 1)))));
 #pragma unroll
-                            for (int j = 0; j < NT; ++j) {
-                                acc[sw][j][0] = fmaf(s0, P[sw][j][0], acc[sw][j][0]);
-                                acc[sw][j][1] = fmaf(s0, P[sw][j][1], acc[sw][j][1]);
-                                acc[sw][j][2] = fmaf(s1, P[sw][j][2], acc[sw][j][2]);
-                                acc[sw][j][3] = fmaf(s1, P[sw][j][3], acc[sw][j][3]);
-                            }
+                        for (int j = 0; j < NT; ++j) {
+                            acc[sw][j][0] = fmaf(s0, P[sw][j][0], acc[sw][j][0]);
+                            acc[sw][j][1] = fmaf(s0, P[sw][j][1], acc[sw][j][1]);
+                            acc[sw][j][2] = fmaf(s1, P[sw][j][2], acc[sw][j][2]);
+                            acc[sw][j][3] = fmaf(s1, P[sw][j][3], acc[sw][j][3]);
                         }
                     }
                 }
-            }
+            };
+            if (ng == kGPC && act[0] && act[1])
+                groups(std::true_type{});
+            else
+                groups(std::false_type{});
 
-            // bias and offset terms of the chunk, (b | s) x (XS | -OFF*XS) / sigma,
-            // taken by the second K half (the first does the final combine)
-            if (kh == 1) {
+            // bias and offset terms of the chunk, (b | s) x (XS | -OFF*XS) / sigma:
+            // K half kh takes slab kh of its pair
 #pragma unroll
-                for (int sw = 0; sw < kSPW; ++sw) {
-                    if (act[sw]) {
-                        uint32_t a0 = *reinterpret_cast<const uint32_t*>(bst + row0[sw] * 8 + 2 * t);
-                        uint32_t a1 = *reinterpret_cast<const uint32_t*>(bst + (row0[sw] + 8) * 8 + 2 * t);
-                        uint32_t a2 = *reinterpret_cast<const uint32_t*>(sst + row0[sw] * 8 + 2 * t);
-                        uint32_t a3 = *reinterpret_cast<const uint32_t*>(sst + (row0[sw] + 8) * 8 + 2 * t);
-                        if (ng < kGPC) {
-                            // groups past the end of K: stale shared memory, zero it
-                            const uint32_t keep = (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
-                            a0 &= keep;
-                            a1 &= keep;
-                            a2 &= keep;
-                            a3 &= keep;
-                        }
+            for (int sw = 0; sw < kSPW; ++sw) {
+                if (sw != kh || !act[sw]) continue;
+                uint32_t a0 = *reinterpret_cast<const uint32_t*>(bst + row0[sw] * 8 + 2 * t);
+                uint32_t a1 = *reinterpret_cast<const uint32_t*>(bst + (row0[sw] + 8) * 8 + 2 * t);
+                uint32_t a2 = *reinterpret_cast<const uint32_t*>(sst + row0[sw] * 8 + 2 * t);
+                uint32_t a3 = *reinterpret_cast<const uint32_t*>(sst + (row0[sw] + 8) * 8 + 2 * t);
+                if (ng < kGPC) {
+                    // groups past the end of K: stale shared memory, zero it
+                    const uint32_t keep = (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
+                    a0 &= keep;
+                    a1 &= keep;
+                    a2 &= keep;
+                    a3 &= keep;
+                }
 #pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            const uint4 bb = xbias[j * 32 + lane];
-                            float D[4];
-                            mma_f16_zc(D, a0, a1, a2, a3, bb.x, bb.y);
-                            mma_f16(D, a0, a1, a2, a3, bb.z, bb.w);
-                            const float2 sg = *reinterpret_cast<const float2*>(xsig + 8 * j + 2 * t);
-                            acc[sw][j][0] = fmaf(sg.x, D[0], acc[sw][j][0]);
-                            acc[sw][j][1] = fmaf(sg.y, D[1], acc[sw][j][1]);
-                            acc[sw][j][2] = fmaf(sg.x, D[2], acc[sw][j][2]);
-                            acc[sw][j][3] = fmaf(sg.y, D[3], acc[sw][j][3]);
-                        }
-                    }
+                for (int j = 0; j < NT; ++j) {
+                    const uint4 bb = xbias[j * 32 + lane];
+                    float D[4];
+                    mma_f16_zc(D, a0, a1, a2, a3, bb.x, bb.y);
+                    mma_f16(D, a0, a1, a2, a3, bb.z, bb.w);
+                    const float2 sg = *reinterpret_cast<const float2*>(xsig + 8 * j + 2 * t);
+                    acc[sw][j][0] = fmaf(sg.x, D[0], acc[sw][j][0]);
+                    acc[sw][j][1] = fmaf(sg.y, D[1], acc[sw][j][1]);
+                    acc[sw][j][2] = fmaf(sg.x, D[2], acc[sw][j][2]);
+                    acc[sw][j][3] = fmaf(sg.y, D[3], acc[sw][j][3]);
                 }
             }
             __syncwarp();
@@ -521,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
         }
         consumer_barrier();
         if (kh == 0) {
-            const BankPtrs bp = p.bank[bank];
+            const BankPtrs bp = P.bank[bank];
 #pragma unroll
             for (int sw = 0; sw < kSPW; ++sw) {
                 if (!act[sw]) continue;
@@ -621,8 +660,11 @@ struct LaunchCfg {
 
 template <int BITS>
 cudaError_t configure_kernels(int group, int mb, int smem_bytes);
+
+// Weight-box width for a format (host side, for encoding tensor maps).
+inline int weight_box_width(int bits, int group) { return wbox_width(bits, group); }
 template <int BITS>
-cudaError_t launch_forward(int group, const LaunchCfg& L, const MainParams& mp);
+cudaError_t launch_forward(int group, const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked);
 template <int BITS>
 cudaError_t launch_unpack(const uint32_t* w, int64_t K, int64_t N, uint8_t* codes, cudaStream_t stream);
 

@@ -4,8 +4,9 @@
 // Work decomposition (one main-kernel CTA per SM):
 //   * K is cut into chunks of kGPC = 8 scale groups; one pipeline stage holds
 //     one chunk for a row block of up to kTN = 128 weight rows: the packed
-//     code bytes of those rows, their 8 scales and 8 biases, and the staged
-//     activation fragments of the chunk.
+//     code bytes of those rows (TMA tensor boxes), their 8 scales and 8 biases
+//     (TMA boxes), and the staged activation fragments of the chunk (one bulk
+//     copy).
 //   * A row block is 8 slabs of 16 rows. There are 8 consumer warps and one
 //     producer warp. Consumer warp w owns slabs (w % 4) and (w % 4) + 4 and
 //     the groups 4*(w / 4) .. 4*(w / 4) + 3 of every chunk, so each slab pair
@@ -54,10 +55,17 @@ QMM_HD constexpr int vblocks_per_chunk(int bits, int group) {
 }
 // Bytes of one weight row that one virtual block consumes.
 QMM_HD constexpr int vblock_bytes(int bits) { return bits == 8 ? 16 : 4 * bits; }
-// Packed bytes of one weight row in a full chunk, and its padded smem stride
-// (stride = 16 mod 32 bytes keeps the 8 row-groups of a warp on distinct banks).
+// Packed bytes of one weight row in a full chunk.
 QMM_HD constexpr int chunk_row_bytes(int bits, int group) { return kGPC * group * bits / 8; }
-QMM_HD constexpr int chunk_row_stride(int bits, int group) { return chunk_row_bytes(bits, group) + 16; }
+// The weight tile of a stage arrives as TMA boxes of kTN rows x W bytes, W the
+// widest of 128/64/32 that divides the chunk row, stored with the matching
+// shared-memory swizzle (16-byte chunk c of row r lands at c ^ f(r)), so every
+// box row is one full-line request and the consumers' reads hit distinct banks.
+QMM_HD constexpr int wbox_width(int bits, int group) {
+    return chunk_row_bytes(bits, group) % 128 == 0 ? 128 : (chunk_row_bytes(bits, group) % 64 == 0 ? 64 : 32);
+}
+QMM_HD constexpr int wbox_count(int bits, int group) { return chunk_row_bytes(bits, group) / wbox_width(bits, group); }
+QMM_HD constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 
 // Staged activations, per chunk: MMA B fragments (one 16-byte vector per lane
 // per virtual block per 8-row tile), the bias-term fragments, and one scale
@@ -71,20 +79,19 @@ QMM_HD constexpr int xprep_chunk_bytes(int bits, int group, int mb) {
     return round_up(xprep_frag_bytes(bits, group, mb) + xprep_bias_bytes(mb) + mb * 4, 128);
 }
 
-// One pipeline stage in shared memory.
-QMM_HD constexpr int stage_weight_bytes(int bits, int group) {
-    return round_up(kTN * chunk_row_stride(bits, group), 128);
-}
+// One pipeline stage in shared memory (1024-byte aligned: the swizzle atom).
+QMM_HD constexpr int stage_weight_bytes(int bits, int group) { return kTN * chunk_row_bytes(bits, group); }
 QMM_HD constexpr int stage_sb_bytes() { return kTN * 16; }   // 8 binary16 values per row
 QMM_HD constexpr int stage_bytes(int bits, int group, int mb) {
-    return stage_weight_bytes(bits, group) + 2 * stage_sb_bytes() + xprep_chunk_bytes(bits, group, mb);
+    return round_up(stage_weight_bytes(bits, group) + 2 * stage_sb_bytes() + xprep_chunk_bytes(bits, group, mb), 1024);
 }
 
 // Scratch for adding the two K halves of every slab pair at a row block's end.
 QMM_HD constexpr int reduce_scratch_bytes(int mb) { return kSlabPairs * kSPW * n8_tiles(mb) * 4 * 32 * 4; }
 // Dynamic shared memory of the main kernel with `stages` pipeline stages.
+// (1024 bytes of slack let the kernel align its stage ring to 1024.)
 QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int stages) {
-    return stages * stage_bytes(bits, group, mb) + stages * 16 + reduce_scratch_bytes(mb);
+    return 1024 + stages * stage_bytes(bits, group, mb) + stages * 16 + reduce_scratch_bytes(mb);
 }
 
 // Offset the unpacked codes carry (128 per bf16 slot; an 8-bit code is
