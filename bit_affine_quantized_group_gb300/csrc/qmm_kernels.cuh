@@ -264,7 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     const MainHeader& p = P.h;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
+    // array so every access below stays a shared-memory access
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int S = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
     uint64_t* empty = full + S;
