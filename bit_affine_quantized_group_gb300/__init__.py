@@ -27,6 +27,8 @@ QMM_ERR_PLAN_MISMATCH = 3
 QMM_ERR_CUDA = 4
 QMM_ERR_ALLOC = 5
 QMM_ERR_TIMEOUT = 6
+QMM_ERR_SCRATCH_LIMIT = 7
+NOALLOC_SCRATCH_BYTES = 4 << 20
 QMM_OUT_F32 = 0
 QMM_OUT_BF16 = 1
 MAX_ROWS = 16
@@ -37,7 +39,7 @@ MAX_SPLITS = 16
 EXPORTS = (
     "qmm_validate_desc", "qmm_workspace_bytes", "qmm_plan", "qmm_plan_get_info",
     "qmm_check_forward_args", "qmm_forward", "qmm_forward_banked", "qmm_unpack_codes",
-    "qmm_plan_error", "qmm_destroy", "qmm_status_string",
+    "qmm_plan_error", "qmm_destroy", "qmm_status_string", "qmm_forward_noalloc",
 )
 
 
@@ -75,6 +77,7 @@ def _load() -> ctypes.CDLL:
     lib.qmm_forward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp]
     lib.qmm_forward_banked.argtypes = [vp, vp, i32, i32, pp, pp, pp, i64, i64, i32, i32, pp, vp]
     lib.qmm_unpack_codes.argtypes = [vp, i64, i64, i32, vp, vp]
+    lib.qmm_forward_noalloc.argtypes = [vp, i32, vp, vp, vp, i64, i64, i32, i32, i32, vp, vp]
     lib.qmm_plan_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.qmm_destroy.argtypes = [vp]
     lib.qmm_destroy.restype = None

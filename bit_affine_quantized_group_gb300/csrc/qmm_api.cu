@@ -174,6 +174,7 @@ const char* qmm_status_string(int status) {
         case QMM_ERR_CUDA: return "QMM_ERR_CUDA: CUDA runtime error";
         case QMM_ERR_ALLOC: return "QMM_ERR_ALLOC: allocation failed";
         case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT: a kernel gave up a bounded wait";
+        case QMM_ERR_SCRATCH_LIMIT: return "QMM_ERR_SCRATCH_LIMIT: the call needs more than the static scratch";
         default: return "unknown qmm status";
     }
 }

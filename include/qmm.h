@@ -69,7 +69,8 @@ enum {
     QMM_ERR_PLAN_MISMATCH = 3, /* K/N/bits/group differ from the plan's */
     QMM_ERR_CUDA = 4,          /* a CUDA runtime call failed (no device, launch error) */
     QMM_ERR_ALLOC = 5,         /* host or device allocation failed in qmm_plan */
-    QMM_ERR_TIMEOUT = 6        /* a kernel gave up a bounded wait (qmm_plan_error) */
+    QMM_ERR_TIMEOUT = 6,       /* a kernel gave up a bounded wait (qmm_plan_error) */
+    QMM_ERR_SCRATCH_LIMIT = 7  /* qmm_forward_noalloc: the call needs more than its static scratch */
 };
 
 /* Output element types. */
@@ -187,6 +188,40 @@ int qmm_unpack_codes(const uint32_t* packed_w, int64_t K, int64_t N, int bits, u
  * QMM_ERR_TIMEOUT in that case.
  */
 int qmm_plan_error(const qmm_plan_t* p, uint32_t* flags);
+
+/*
+ * Size of the device scratch qmm_forward_noalloc keeps in a static device
+ * array (held by every GPU that loads this library until the process exits).
+ */
+#define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * qmm_forward without a plan and without any allocation, for callers that
+ * cannot call cudaMalloc when they run a projection (code that runs while
+ * another component owns the device allocator, loops that forbid allocation
+ * after start-up, plug-in hosts that only hand over their tensors). The pages
+ * describe no counterpart: this is a deployment variant of qmm_forward.
+ *
+ * Same arguments and data layout as qmm_forward, with the output type given
+ * directly (QMM_OUT_F32 or QMM_OUT_BF16) and splits fixed at 1. The per-call
+ * activation staging lives in a static device array of
+ * QMM_NOALLOC_SCRATCH_BYTES; a call whose staging would not fit returns
+ * QMM_ERR_SCRATCH_LIMIT before touching the device (with 9..16 rows the
+ * largest K is 114688 for 4/5/6-bit codes in groups of 32, 122368 in groups of
+ * 64, and 61184 / 62976 for 8-bit codes; with 1..8 rows about twice that). Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ * The first call on a device (with that device current) looks up the
+ * scratch's device address and sets the kernels' shared-memory limit; make
+ * that first call before any stream capture. Every call on a device shares the
+ * one scratch array and overwrites it, so calls whose executions overlap on
+ * the GPU (different streams, or concurrent host threads) race: serialize
+ * them. Device-side timeouts are recorded only in the scratch and not
+ * reported; use qmm_forward for that.
+ */
+int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* packed_w, const uint16_t* scales_f16,
+                        const uint16_t* biases_f16, int64_t K, int64_t N, int bits, int group, int out_dtype,
+                        void* out, void* stream);
 
 /* Free the plan and any workspace it allocated. NULL is accepted. */
 void qmm_destroy(qmm_plan_t* p);

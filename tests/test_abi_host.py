@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(q):
 
 
 def test_status_strings(q):
-    for st in range(7):
+    for st in range(8):
         assert q.status_string(st).startswith("QMM_")
     assert q.status_string(99) == "unknown qmm status"
 
