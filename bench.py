@@ -42,7 +42,8 @@ METRIC = "qmm effective HBM GB/s (codes+scales+biases+x+y bytes / time), M=1,2,4
 # dram__bytes_write.sum) on this workload, keyed by M, and the hash of the
 # kernel sources they were measured on. If the sources change, traffic is
 # reported as null until re-measured.
-TRAFFIC = {"source_sha": None, "per_M": {}}
+TRAFFIC = {"source_sha": "2dcd9a403dc69461",
+           "per_M": {"1": 55863552, "2": 55863552, "4": 55863808, "8": 55863808, "16": 55964160}}
 
 
 def kernel_source_sha() -> str:
