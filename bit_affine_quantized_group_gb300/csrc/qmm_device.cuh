@@ -189,28 +189,33 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 // term (sum x*(128+q) = P + 128*XS).
 constexpr uint32_t kBf16x2_128 = 0x43004300u;
 
+// `magic` is kBf16x2_128, passed in as a run-time value by the hot loop: a
+// three-input logic op takes a single immediate, so with both the mask and the
+// pattern as literals every (w & mask) | pattern would compile to two ops.
+
 // 4-bit (and each word of an 8-bit row read as 8 nibbles): one word holds the
 // lane's 8 codes, nibble i = code i.
-__device__ __forceinline__ void unpack_nibbles(uint32_t w, uint32_t (&r)[4]) {
+__device__ __forceinline__ void unpack_nibbles(uint32_t w, uint32_t (&r)[4], uint32_t magic = kBf16x2_128) {
     constexpr uint32_t m = 0x000F000Fu;
-    r[0] = (w & m) | kBf16x2_128;
-    r[1] = ((w >> 4) & m) | kBf16x2_128;
-    r[2] = ((w >> 8) & m) | kBf16x2_128;
-    r[3] = ((w >> 12) & m) | kBf16x2_128;
+    r[0] = (w & m) | magic;
+    r[1] = ((w >> 4) & m) | magic;
+    r[2] = ((w >> 8) & m) | magic;
+    r[3] = ((w >> 12) & m) | magic;
 }
 
 // 5- or 6-bit: the lane's 8 codes are 5 or 6 bytes starting at byte BITS*t of
 // the block; `lo`, `hi` are the two words covering them and `sh` (0, 8, 16,
 // 24) the bit offset of the first code inside `lo`.
 template <int BITS>
-__device__ __forceinline__ void unpack_odd(uint32_t lo, uint32_t hi, uint32_t sh, uint32_t (&r)[4]) {
+__device__ __forceinline__ void unpack_odd(uint32_t lo, uint32_t hi, uint32_t sh, uint32_t (&r)[4],
+                                           uint32_t magic = kBf16x2_128) {
     const uint64_t v = ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
     constexpr uint32_t mk = (1u << BITS) - 1u;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t a = static_cast<uint32_t>(v >> (BITS * i)) & mk;
         const uint32_t b = static_cast<uint32_t>(v >> (BITS * (i + 4))) & mk;
-        r[i] = a | (b << 16) | kBf16x2_128;
+        r[i] = a | (b << 16) | magic;
     }
 }
 

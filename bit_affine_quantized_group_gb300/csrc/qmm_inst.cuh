@@ -18,26 +18,27 @@ cudaError_t configure_one(int smem_bytes) {
 
 template <int BITS, int GROUP, int MB, int CAP>
 cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
-    // (1) activation staging: ordinary stream order after the caller's work.
+    // Both kernels are programmatic dependents of what precedes them on the
+    // stream: each may be scheduled while its predecessor still runs and waits
+    // (griddepcontrol.wait) before touching anything the predecessor produces.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // (1) activation staging
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(mp.h.C));
     cfg.blockDim = dim3(kXprepThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = L.stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_xprep_kernel<BITS, GROUP, MB>, L.x, L.M, mp.h.K, mp.h.G,
                                        const_cast<uint8_t*>(mp.h.xprep));
     if (e != cudaSuccess) return e;
-    // (2) main kernel as a programmatic dependent of (1).
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // (2) main kernel: loads weights at once, waits for (1) before its staged activations
     cfg.gridDim = dim3(static_cast<unsigned>(L.ctas));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP>, mp);
 }
 

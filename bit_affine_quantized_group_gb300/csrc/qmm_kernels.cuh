@@ -69,6 +69,7 @@ struct MainHeader {
     int sb_tma;             // scales/biases by TMA boxes (G % 8 == 0), else cp.async
     int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
     int banks;
+    uint32_t unpack_magic;  // kBf16x2_128, given at run time so it stays in a register
 };
 
 template <int CAP>
@@ -142,10 +143,14 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
     constexpr float OFF = code_offset(BITS);
 
-    // The main kernel may start loading weights while this runs.
+    // The main kernel may start loading weights while this runs. This kernel is
+    // itself launched as a programmatic dependent of whatever ran before it on the
+    // stream, so it must wait for that work (which may produce x, or still read
+    // the staging buffer) before touching x or the buffer.
     griddep_launch_dependents();
+    griddep_wait();
 
-    __shared__ uint16_t xs[MB][CK];
+    __shared__ __align__(16) uint16_t xs[MB][CK];
     __shared__ float xsum[MB][kGPC];
     __shared__ float rsig[MB];     // 1 / sigma
     __shared__ float sig[MB];
@@ -157,9 +162,30 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     const int kc = ng * GROUP;
     const int tid = threadIdx.x;
 
-    for (int i = tid; i < MB * CK; i += blockDim.x) {
-        const int m = i / CK, k = i - (i / CK) * CK;
-        xs[m][k] = (m < M && k < kc) ? x[static_cast<int64_t>(m) * K + k0 + k] : static_cast<uint16_t>(0);
+    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        // rows are 2K bytes apart and chunks start 16-byte aligned: 16-byte loads,
+        // all issued before any is used
+        constexpr int V8 = CK / 8;                          // 16-byte pieces per row
+        constexpr int PER = (MB * V8 + kXprepThreads - 1) / kXprepThreads;
+        uint4 v[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int i = tid + u * kXprepThreads;
+            const int m = i / V8, kk = (i - (i / V8) * V8) * 8;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (i < MB * V8 && m < M && kk < kc)
+                v[u] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(m) * K + k0 + kk);
+        }
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int i = tid + u * kXprepThreads;
+            if (i < MB * V8) reinterpret_cast<uint4*>(&xs[0][0])[i] = v[u];
+        }
+    } else {
+        for (int i = tid; i < MB * CK; i += blockDim.x) {
+            const int m = i / CK, k = i - (i / CK) * CK;
+            xs[m][k] = (m < M && k < kc) ? x[static_cast<int64_t>(m) * K + k0 + k] : static_cast<uint16_t>(0);
+        }
     }
     __syncthreads();
     if (tid < MB * kGPC) {
@@ -301,6 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
         const uint32_t tx_stage =
             static_cast<uint32_t>(NBOX * kTN * W + (p.sb_tma ? 2 * SSB : 0) + XPB);
         uint32_t it = 0;
+        int pslot = 0;            // it % S, kept incrementally (S is a run-time value)
+        uint32_t pround = 0;      // it / S
         bool waited = false;
         bool ok = true;
         int npend = 0;
@@ -332,11 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                  ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & 3) == 0);
             if (!sb_ok && lane == 0) record_bad_copy(p.err, bp.s, static_cast<uint64_t>(rows), 4u);
             for (int c = c0; c < c1; ++c) {
-                const int slot = static_cast<int>(it % S);
+                const int slot = pslot;
                 // After a timed-out wait the error is recorded and no further waits are
                 // made; the loop still runs to the end so that every warp finishes.
+                // (The slot's previous use was in round pround - 1: parity pround ^ 1.)
                 if (it >= static_cast<uint32_t>(S) && ok &&
-                    !mbar_wait(&empty[slot], ((it / S) - 1) & 1u, p.err, kErrEmptyWait))
+                    !mbar_wait(&empty[slot], (pround ^ 1u) & 1u, p.err, kErrEmptyWait))
                     ok = false;
                 uint8_t* st = smem + slot * SB;
                 if (lane == 0) {
@@ -373,6 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                     if (++npend == S) flush_pending();
                 }
                 ++it;
+                if (++pslot == S) {
+                    pslot = 0;
+                    ++pround;
+                }
             }
             return true;
         });
@@ -389,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     }
 
     // -------------------------------- consumers --------------------------------
+    const uint32_t magic = p.unpack_magic;
     const int g = lane >> 2;
     const int t = lane & 3;
     const int sp = warp % kSlabPairs;        // slabs sp and sp + 4
@@ -406,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
         else
             cx[i] = 0;
     }
-    uint32_t it = 0;
+    int cslot = 0;            // stage index % S, kept incrementally
+    uint32_t cphase = 0;      // (stage index / S) & 1
     bool ok = true;
     for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
         const int nsl = (rows + kSlab - 1) / kSlab;
@@ -427,10 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                 for (int e = 0; e < 4; ++e) acc[sw][j][e] = 0.0f;
 
         for (int c = c0; c < c1; ++c) {
-            const int slot = static_cast<int>(it % S);
+            const int slot = cslot;
             // a timed-out wait is recorded; the warp then stops waiting but keeps the
             // same control flow, so the consumer barriers below are always reached
-            if (ok && !mbar_wait(&full[slot], (it / S) & 1u, p.err, kErrFullWait)) ok = false;
+            if (ok && !mbar_wait(&full[slot], cphase, p.err, kErrFullWait)) ok = false;
             const int ng = min(kGPC, p.G - c * kGPC);
             const uint8_t* st = smem + slot * SB;
             const uint8_t* wst = st;
@@ -471,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                             uint32_t ra[4], rb[4];
                             if constexpr (BITS == 4 || BITS == 8) {
                                 const uint8_t* a0 = wst + (row0[sw] - g) * W + cx[vi];
-                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + g * W), ra);
-                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + (g + 8) * W), rb);
+                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + g * W), ra, magic);
+                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + (g + 8) * W), rb, magic);
                             } else {
                                 const int b0 = vb * BB + 4 * odd_word<BITS>(t);
                                 const int r0 = row0[sw], r1 = row0[sw] + 8;
@@ -480,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                                 const uint32_t hi0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r0, b0 + 4));
                                 const uint32_t lo1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r1, b0));
                                 const uint32_t hi1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r1, b0 + 4));
-                                unpack_odd<BITS>(lo0, hi0, odd_shift<BITS>(t), ra);
-                                unpack_odd<BITS>(lo1, hi1, odd_shift<BITS>(t), rb);
+                                unpack_odd<BITS>(lo0, hi0, odd_shift<BITS>(t), ra, magic);
+                                unpack_odd<BITS>(lo1, hi1, odd_shift<BITS>(t), rb, magic);
                             }
 #pragma unroll
                             for (int j = 0; j < NT; ++j) {
@@ -547,7 +582,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            ++it;
+            if (++cslot == S) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
         }
 
         // combine the two K halves in a fixed order: (first half) + (second half)
