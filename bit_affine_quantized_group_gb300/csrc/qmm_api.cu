@@ -341,7 +341,7 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
     h.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
     h.sb_tma = (p->G % 8 == 0) ? 1 : 0;
     h.sb_vec16 = h.sb_tma;
-    h.unpack_magic = kBf16x2_128;
+    h.unpack_magic = kF16x2_1024;
     h.banks = n_banks;
     h.xprep_bytes = static_cast<int64_t>(p->C) * xprep_chunk_bytes(bits, group, mi == 0 ? 8 : 16);
     h.rows_total = static_cast<int64_t>(n_banks) * p->splits * N;

@@ -1,6 +1,6 @@
 // Device primitives for the qmm kernels (sm_103a): inline PTX for mbarriers,
 // bulk (TMA) and cp.async copies, programmatic dependent launch, the warp-level
-// bf16 / f16 tensor-core MMA, and the in-register code unpackers.
+// binary16 tensor-core MMA, and the in-register code unpackers.
 #pragma once
 
 #include <cuda.h>
@@ -146,23 +146,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 }
 
 // ---- tensor-core MMA (warp level) -------------------------------------------
-// D = A*B + C, m16n8k16, A/B bf16, C/D fp32.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// D = A*B (zero accumulator), m16n8k16, A/B bf16.
-__device__ __forceinline__ void mma_bf16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                            uint32_t b0, uint32_t b1) {
-    const float z = 0.0f;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
-}
 // D = A*B (zero accumulator), m16n8k16, A/B binary16.
 __device__ __forceinline__ void mma_f16_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                            uint32_t b0, uint32_t b1) {
@@ -172,7 +155,7 @@ __device__ __forceinline__ void mma_f16_zc(float (&d)[4], uint32_t a0, uint32_t 
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
-// Same with binary16 operands.
+// D = A*B + C, m16n8k16, A/B binary16, C/D fp32.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
@@ -182,25 +165,56 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 }
 
 // ---- code unpacking ----------------------------------------------------------
-// Every unpacker produces four bf16x2 registers r[i] = (128 + c_i, 128 + c_{i+4})
-// for the 8 codes c_0..c_7 a lane owns in one virtual k32 block. A code q < 128
-// written into the low mantissa bits of the bf16 pattern 0x4300 (= 128.0) is
-// the exact value 128 + q; the 128 offset is removed later through the bias
-// term (sum x*(128+q) = P + 128*XS).
-constexpr uint32_t kBf16x2_128 = 0x43004300u;
+// Every unpacker turns the 8 codes c_0..c_7 a lane owns in one k32 block into
+// four binary16x2 registers. A code q placed at bits j..j+bits-1 of the
+// mantissa of the binary16 pattern 0x6400 (= 1024.0) is the exact value
+// 1024 + q * 2^j (the mantissa has 10 bits). Register r, half h holds code
+// slot_code(r, h) with shift slot_shift(r, h); the staged activation in the
+// same slot is multiplied by 2^-j, so each product is x * q plus an offset
+// x * 1024 * 2^-j that the bias term removes exactly.
+constexpr uint32_t kF16x2_1024 = 0x64006400u;
 
-// `magic` is kBf16x2_128, passed in as a run-time value by the hot loop: a
+// `magic` is kF16x2_1024, passed in as a run-time value by the hot loop: a
 // three-input logic op takes a single immediate, so with both the mask and the
 // pattern as literals every (w & mask) | pattern would compile to two ops.
 
-// 4-bit (and each word of an 8-bit row read as 8 nibbles): one word holds the
-// lane's 8 codes, nibble i = code i.
-__device__ __forceinline__ void unpack_nibbles(uint32_t w, uint32_t (&r)[4], uint32_t magic = kBf16x2_128) {
-    constexpr uint32_t m = 0x000F000Fu;
-    r[0] = (w & m) | magic;
-    r[1] = ((w >> 4) & m) | magic;
-    r[2] = ((w >> 8) & m) | magic;
-    r[3] = ((w >> 12) & m) | magic;
+// Slot tables: which of the lane's 8 codes, and its mantissa shift j.
+QMM_HD constexpr int slot_code(int bits, int r, int h) {
+    return bits == 4 ? (h == 0 ? r : r + 4)
+         : bits == 8 ? ((r >> 1) * 4 + (r & 1) + 2 * h)
+         : bits == 5 ? (h == 0 ? r : r + 4)
+         : /* 6 */     (r < 3 ? (h == 0 ? r : r + 3) : 6 + h);
+}
+QMM_HD constexpr int slot_shift(int bits, int r, int h) {
+    return bits == 4 ? ((r & 1) ? 4 : 0)
+         : bits == 8 ? 0
+         : bits == 5 ? (h == 0 ? 0 : 4)
+         : /* 6 */     ((r < 3 && h == 1) ? 2 : 0);
+}
+// Shift j of the lane's code i (the inverse view of the tables).
+QMM_HD constexpr int code_shift(int bits, int i) {
+    return bits == 4 ? ((i & 1) ? 4 : 0)
+         : bits == 8 ? 0
+         : bits == 5 ? (i < 4 ? 0 : 4)
+         : /* 6 */     ((i >= 3 && i <= 5) ? 2 : 0);
+}
+
+// 4-bit: one word holds the lane's 8 codes, nibble i = code i.
+__device__ __forceinline__ void unpack4(uint32_t w, uint32_t (&r)[4], uint32_t magic = kF16x2_1024) {
+    r[0] = (w & 0x000F000Fu) | magic;          // c0, c4          (shift 0)
+    r[1] = (w & 0x00F000F0u) | magic;          // c1, c5          (shift 4)
+    const uint32_t w8 = w >> 8;
+    r[2] = (w8 & 0x000F000Fu) | magic;         // c2, c6
+    r[3] = (w8 & 0x00F000F0u) | magic;         // c3, c7
+}
+
+// 8-bit: two words hold the lane's 8 codes, byte i = code i.
+__device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t (&r)[4],
+                                        uint32_t magic = kF16x2_1024) {
+    r[0] = (w0 & 0x00FF00FFu) | magic;         // c0, c2
+    r[1] = ((w0 >> 8) & 0x00FF00FFu) | magic;  // c1, c3
+    r[2] = (w1 & 0x00FF00FFu) | magic;         // c4, c6
+    r[3] = ((w1 >> 8) & 0x00FF00FFu) | magic;  // c5, c7
 }
 
 // 5- or 6-bit: the lane's 8 codes are 5 or 6 bytes starting at byte BITS*t of
@@ -208,28 +222,34 @@ __device__ __forceinline__ void unpack_nibbles(uint32_t w, uint32_t (&r)[4], uin
 // 24) the bit offset of the first code inside `lo`.
 template <int BITS>
 __device__ __forceinline__ void unpack_odd(uint32_t lo, uint32_t hi, uint32_t sh, uint32_t (&r)[4],
-                                           uint32_t magic = kBf16x2_128) {
+                                           uint32_t magic = kF16x2_1024) {
     const uint64_t v = ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
-    constexpr uint32_t mk = (1u << BITS) - 1u;
+    if constexpr (BITS == 5) {
+        // c_i at bit 0 and c_{i+4} at bit 20 (= 16 + 4) of the same window
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t a = static_cast<uint32_t>(v >> (BITS * i)) & mk;
-        const uint32_t b = static_cast<uint32_t>(v >> (BITS * (i + 4))) & mk;
-        r[i] = a | (b << 16) | magic;
+        for (int i = 0; i < 4; ++i) r[i] = (static_cast<uint32_t>(v >> (5 * i)) & 0x01F0001Fu) | magic;
+    } else {
+        // c_i at bit 0 and c_{i+3} at bit 18 (= 16 + 2); c6 and c7 from two windows
+#pragma unroll
+        for (int i = 0; i < 3; ++i) r[i] = (static_cast<uint32_t>(v >> (6 * i)) & 0x00FC003Fu) | magic;
+        r[3] = (static_cast<uint32_t>(v >> 36) & 0x3Fu) | (static_cast<uint32_t>(v >> 26) & 0x003F0000u) | magic;
     }
 }
 
-// Word index (within a virtual block) and bit shift of lane t's codes for odd widths.
+// Word index (within a k32 block) and bit shift of lane t's codes for odd widths.
 template <int BITS>
 __device__ __forceinline__ int odd_word(int t) { return (BITS * t) >> 2; }
 template <int BITS>
 __device__ __forceinline__ uint32_t odd_shift(int t) { return static_cast<uint32_t>(((BITS * t) & 3) * 8); }
 
-// Unpack lane t's 8 codes of the virtual block starting at `blk` (4-byte aligned).
+// Unpack lane t's 8 codes of the k32 block starting at `blk` (4-byte aligned,
+// 8-byte aligned for 8-bit codes). Used by the unpack diagnostic.
 template <int BITS>
 __device__ __forceinline__ void unpack_block(const uint32_t* blk, int t, uint32_t (&r)[4]) {
-    if constexpr (BITS == 4 || BITS == 8) {
-        unpack_nibbles(blk[t], r);
+    if constexpr (BITS == 4) {
+        unpack4(blk[t], r);
+    } else if constexpr (BITS == 8) {
+        unpack8(blk[2 * t], blk[2 * t + 1], r);
     } else {
         const int w = odd_word<BITS>(t);
         unpack_odd<BITS>(blk[w], blk[w + 1], odd_shift<BITS>(t), r);

@@ -71,7 +71,7 @@ template <>
 cudaError_t launch_unpack<QMM_INST_BITS>(const uint32_t* w, int64_t K, int64_t N, uint8_t* codes,
                                           cudaStream_t stream) {
     constexpr int B = QMM_INST_BITS;
-    const int64_t vbk = (B == 8) ? K / 16 : K / 32;
+    const int64_t vbk = K / 32;
     const int64_t total = N * vbk * 4;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 65535) blocks = 65535;

@@ -21,13 +21,18 @@
 //                            partials in slice order (same page, "JANGH split-K
 //                            verify tile" commit: FP32 partials, then a sum).
 //
-// Per scale group g the main kernel forms, with 128-offset codes A = 128 + q,
-//   P'[m,n,g] = sum_{k in g} x[m,k] * A[n,k] = P + 128*XS
-// (for 8-bit codes, split into nibbles lo + 16*hi, P' = P + 2176*XS) and then
-//   y += s*P' + (b - OFF*s)*XS,      OFF = 128 (2176 for 8-bit),
+// Per scale group g the main kernel forms, with the unpacked binary16 weights
+// A[n,k] = 1024 + q[n,k] * 2^j(k) and the staged activations
+// x'[m,k] = f[m,c] * x[m,k] * 2^-j(k) (f a power-of-two range factor per
+// activation row and 8-group chunk c, j(k) the code's mantissa shift),
+//   P'[m,n,g] = sum_{k in g} x'[m,k] * A[n,k] = f * (P + XSc),
+//   XSc[m,g]  = sum_{k in g} x[m,k] * 1024 * 2^-j(k),
+// and then
+//   y += (1/f) * sum_g s*P'  +  sum_g (b*XS - s*XSc),
 // which is  sum_g s*P + b*XS.  The s*P' part is one FMA per accumulator per
-// group; the (b, s) x (XS, -OFF*XS) part is a small binary16 MMA per 8-group
-// chunk, with XS split into high and low binary16 halves so it keeps ~22 bits.
+// group (plus one per chunk for 1/f); the (b, s) x (XS, -XSc) part is a small
+// binary16 MMA per chunk, with XS and XSc split into high and low binary16
+// halves so each keeps ~22 bits.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -122,16 +127,10 @@ __device__ __forceinline__ void for_each_row_block(const MainHeader& p, F&& f) {
 // ---------------------------------------------------------------------------
 // 1. Activation staging.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo, uint16_t hi) {
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-__device__ __forceinline__ uint16_t bf16_times16(uint16_t v) {
-    const float f = __bfloat162float(__ushort_as_bfloat16(v)) * 16.0f;   // exact (power of two)
-    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
 }
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t v) { return __uint_as_float(v << 16); }
 
 template <int BITS, int GROUP, int MB>
 __global__ void __launch_bounds__(kXprepThreads)
@@ -141,7 +140,6 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     constexpr int NT = n8_tiles(MB);
     constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
     constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
-    constexpr float OFF = code_offset(BITS);
 
     // The main kernel may start loading weights while this runs. This kernel is
     // itself launched as a programmatic dependent of whatever ran before it on the
@@ -151,9 +149,11 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     griddep_wait();
 
     __shared__ __align__(16) uint16_t xs[MB][CK];
-    __shared__ float xsum[MB][kGPC];
-    __shared__ float rsig[MB];     // 1 / sigma
-    __shared__ float sig[MB];
+    __shared__ float xsum[MB][kGPC];     // XS
+    __shared__ float xsc[MB][kGPC];      // XSc
+    __shared__ uint32_t xmag[MB][kGPC];  // largest |x| bit pattern of the group
+    __shared__ float rsig[MB];           // 1 / sigma
+    __shared__ float fsc[MB];            // f
 
     const int c = blockIdx.x;
     const int g0 = c * kGPC;
@@ -189,49 +189,76 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     }
     __syncthreads();
     if (tid < MB * kGPC) {
+        // XS, XSc and the largest magnitude of one (row, group), 8 codes at a time
+        // (code k of a k32 block has mantissa shift j = code_shift(k % 8))
         const int m = tid / kGPC, gg = tid % kGPC;
-        float s = 0.0f;
-        for (int k = 0; k < GROUP; ++k) s += __bfloat162float(__ushort_as_bfloat16(xs[m][gg * GROUP + k]));
+        float s = 0.0f, sc = 0.0f;
+        uint32_t mag = 0;
+        const uint4* src = reinterpret_cast<const uint4*>(&xs[m][gg * GROUP]);
+#pragma unroll
+        for (int u = 0; u < GROUP / 8; ++u) {
+            const uint4 q = src[u];
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t hbits = (wv[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+                const float xv = bf16_bits_to_float(hbits);
+                s += xv;
+                sc = fmaf(xv, 1024.0f / static_cast<float>(1 << code_shift(BITS, e)), sc);
+                mag = max(mag, hbits & 0x7FFFu);
+            }
+        }
         xsum[m][gg] = s;
+        xsc[m][gg] = sc;
+        xmag[m][gg] = mag;
     }
     __syncthreads();
     if (tid < MB) {
         float amax = 0.0f;
-        for (int gg = 0; gg < kGPC; ++gg) amax = fmaxf(amax, fabsf(xsum[tid][gg]));
-        amax *= OFF;
-        // sigma = 2^(e-13) puts the largest |OFF*XS/sigma| in [2^13, 2^14):
+        uint32_t mag = 0;
+        for (int gg = 0; gg < kGPC; ++gg) {
+            amax = fmaxf(amax, fmaxf(fabsf(xsum[tid][gg]), fabsf(xsc[tid][gg])));
+            mag = max(mag, xmag[tid][gg]);
+        }
+        // sigma = 2^(e-13) puts the largest |XS/sigma|, |XSc/sigma| in [2^13, 2^14):
         // inside the binary16 range with room to spare.
         float sg = 1.0f;
         if (amax > 0.0f && amax <= 3.0e38f) sg = ldexpf(1.0f, ilogbf(amax) - 13);
-        sig[tid] = sg;
         rsig[tid] = 1.0f / sg;    // exact: power of two
+        // f = 2^(14 - e), e the binary exponent of the chunk's largest |x| (read
+        // off its bf16 bit pattern; clamped so f and 1/f stay normal floats):
+        // every f*x*2^-j is then below 2^15, and any x within 2^27 of the
+        // largest is exact in binary16.
+        int e = 0;
+        if (mag != 0) e = min(127, max(-100, static_cast<int>(mag >> 7) - 127));
+        const float f = (mag != 0) ? ldexpf(1.0f, 14 - e) : 1.0f;
+        fsc[tid] = f;
+        float* tail = reinterpret_cast<float*>(xprep + static_cast<size_t>(c) * XPB + XFB + xprep_bias_bytes(MB));
+        tail[tid] = sg;
+        tail[MB + tid] = 1.0f / f;  // exact: power of two
     }
     __syncthreads();
 
     uint8_t* out = xprep + static_cast<size_t>(c) * XPB;
     uint4* frag = reinterpret_cast<uint4*>(out);
     for (int i = tid; i < KB * NT * 32; i += blockDim.x) {
+        // lane (g, t) of 8-row tile j, k32 block vb: activation row 8j + g,
+        // codes 32vb + 8t .. 32vb + 8t + 7 in the unpackers' slot order
         const int lane = i & 31;
         const int j = (i >> 5) % NT;
         const int vb = (i >> 5) / NT;
         const int t = lane & 3;
         const int m = 8 * j + (lane >> 2);
+        const int kb = 32 * vb + 8 * t;
+        const float f = fsc[m];
         uint32_t r[4];
-        if constexpr (BITS == 8) {
-            // virtual block vb = real codes 16*vb .. 16*vb+15; lane t holds the
-            // word with real codes kb..kb+3; its nibble slots pair (lo q0, lo q2),
-            // (hi q0, hi q2), (lo q1, lo q3), (hi q1, hi q3); hi nibbles weigh 16.
-            const int kb = 16 * vb + 4 * t;
-            const uint16_t a0 = xs[m][kb], a1 = xs[m][kb + 1], a2 = xs[m][kb + 2], a3 = xs[m][kb + 3];
-            r[0] = pack_bf16x2(a0, a2);
-            r[1] = pack_bf16x2(bf16_times16(a0), bf16_times16(a2));
-            r[2] = pack_bf16x2(a1, a3);
-            r[3] = pack_bf16x2(bf16_times16(a1), bf16_times16(a3));
-        } else {
-            // lane t owns codes 8t..8t+7 of the k32 block; slot pair i is (c_i, c_{i+4}).
-            const int kb = 32 * vb + 8 * t;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) r[q] = pack_bf16x2(xs[m][kb + q], xs[m][kb + q + 4]);
+        for (int q = 0; q < 4; ++q) {
+            const float lo = bf16_bits_to_float(xs[m][kb + slot_code(BITS, q, 0)]) * f *
+                             (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 0)));
+            const float hi = bf16_bits_to_float(xs[m][kb + slot_code(BITS, q, 1)]) * f *
+                             (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 1)));
+            r[q] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
         }
         frag[i] = make_uint4(r[0], r[1], r[2], r[3]);
     }
@@ -243,15 +270,14 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
         const int m = 8 * j + (lane >> 2);
         const float v0 = xsum[m][2 * t] * rsig[m];
         const float v1 = xsum[m][2 * t + 1] * rsig[m];
-        const float w0 = -OFF * v0;
-        const float w1 = -OFF * v1;
+        const float w0 = -xsc[m][2 * t] * rsig[m];
+        const float w1 = -xsc[m][2 * t + 1] * rsig[m];
         const __half v0h = __float2half_rn(v0), v1h = __float2half_rn(v1);
         const __half w0h = __float2half_rn(w0), w1h = __float2half_rn(w1);
         const __half v0l = __float2half_rn(v0 - __half2float(v0h)), v1l = __float2half_rn(v1 - __half2float(v1h));
         const __half w0l = __float2half_rn(w0 - __half2float(w0h)), w1l = __float2half_rn(w1 - __half2float(w1h));
         bias[i] = make_uint4(pack_half2(v0h, v1h), pack_half2(w0h, w1h), pack_half2(v0l, v1l), pack_half2(w0l, w1l));
     }
-    if (tid < MB) reinterpret_cast<float*>(out + XFB + xprep_bias_bytes(MB))[tid] = sig[tid];
 }
 
 // ---------------------------------------------------------------------------
@@ -286,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
     constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
     constexpr int SB = stage_bytes(BITS, GROUP, MB);
-    constexpr int NV = kGroupsPerWarp * VB;        // virtual blocks per consumer warp per stage
+    constexpr int NV = kGroupsPerWarp * VB;        // k32 blocks per consumer warp per stage
     const MainHeader& p = P.h;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -429,14 +455,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     const int kh = warp / kSlabPairs;        // chunk groups 4*kh .. 4*kh + 3
     const int gbase = kh * kGroupsPerWarp;
     const int vbw = gbase * VB;              // first virtual block of this warp in a chunk
-    // Offsets of this lane's word in each of the warp's virtual blocks, for a
-    // tile row r with r % 8 == 0 (add r * W): box base + swizzled 16-byte chunk.
-    // Valid for the 4-bit and 8-bit layouts (128-byte boxes, one word per block).
+    // Offsets of this lane's codes in each of the warp's k32 blocks, for a tile
+    // row r with r % 8 == 0 (add r * W): box base + swizzled 16-byte chunk +
+    // byte. 4-bit: one word (block = one 16-byte chunk); 8-bit: two words
+    // (block = two chunks). Both use 128-byte boxes.
     int cx[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
-        if constexpr (BITS == 4 || BITS == 8)
-            cx[i] = (((vbw + i) >> 3) << 14) + (((((vbw + i) & 7) ^ g) << 4) | (4 * t));
+        const int vb = vbw + i;
+        if constexpr (BITS == 4)
+            cx[i] = ((vb >> 3) << 14) + ((((vb & 7) ^ g) << 4) | (4 * t));
+        else if constexpr (BITS == 8)
+            cx[i] = ((vb >> 2) << 14) + (((((2 * vb + (t >> 1)) & 7) ^ g) << 4) | (8 * (t & 1)));
         else
             cx[i] = 0;
     }
@@ -474,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
             const uint4* xfr = reinterpret_cast<const uint4*>(st + SW + 2 * SSB);
             const uint4* xbias = reinterpret_cast<const uint4*>(st + SW + 2 * SSB + XFB);
             const float* xsig = reinterpret_cast<const float*>(st + SW + 2 * SSB + XFB + xprep_bias_bytes(MB));
+            const float* xrf = xsig + MB;            // 1/f per activation row
 
             // this warp's 4 scales for each of its slab rows (binary16 pairs)
             uint2 sv0[kSPW], sv1[kSPW];
@@ -487,8 +518,18 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
             // case (full chunk, both slabs live) so loads of later groups can be
             // scheduled under the tensor-core work of earlier ones, and guarded for
             // partial chunks and partial row blocks.
+            // Per-chunk sums sum_g s*P' (still scaled by f), folded into acc with 1/f.
+            float accc[kSPW][NT][4];
             auto groups = [&](auto full_tag) {
                 constexpr bool FULL = decltype(full_tag)::value;
+                if constexpr (!FULL) {
+#pragma unroll
+                    for (int sw = 0; sw < kSPW; ++sw)
+#pragma unroll
+                        for (int j = 0; j < NT; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) accc[sw][j][e] = 0.0f;
+                }
 #pragma unroll
                 for (int gl = 0; gl < kGroupsPerWarp; ++gl) {
                     if (!FULL && gbase + gl >= ng) continue;
@@ -504,10 +545,16 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                         for (int sw = 0; sw < kSPW; ++sw) {
                             if (!FULL && !act[sw]) continue;
                             uint32_t ra[4], rb[4];
-                            if constexpr (BITS == 4 || BITS == 8) {
+                            if constexpr (BITS == 4) {
                                 const uint8_t* a0 = wst + (row0[sw] - g) * W + cx[vi];
-                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + g * W), ra, magic);
-                                unpack_nibbles(*reinterpret_cast<const uint32_t*>(a0 + (g + 8) * W), rb, magic);
+                                unpack4(*reinterpret_cast<const uint32_t*>(a0 + g * W), ra, magic);
+                                unpack4(*reinterpret_cast<const uint32_t*>(a0 + (g + 8) * W), rb, magic);
+                            } else if constexpr (BITS == 8) {
+                                const uint8_t* a0 = wst + (row0[sw] - g) * W + cx[vi];
+                                const uint2 u0 = *reinterpret_cast<const uint2*>(a0 + g * W);
+                                const uint2 u1 = *reinterpret_cast<const uint2*>(a0 + (g + 8) * W);
+                                unpack8(u0.x, u0.y, ra, magic);
+                                unpack8(u1.x, u1.y, rb, magic);
                             } else {
                                 const int b0 = vb * BB + 4 * odd_word<BITS>(t);
                                 const int r0 = row0[sw], r1 = row0[sw] + 8;
@@ -521,10 +568,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
 #pragma unroll
                             for (int j = 0; j < NT; ++j) {
                                 if (v == 0)
-                                    mma_bf16_zc(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                    mma_f16_zc(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
                                 else
-                                    mma_bf16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
-                                mma_bf16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
+                                    mma_f16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
+                                mma_f16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
                             }
                         }
                     }
@@ -537,10 +584,17 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                         const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (gl & 1)))));
 #pragma unroll
                         for (int j = 0; j < NT; ++j) {
-                            acc[sw][j][0] = fmaf(s0, P[sw][j][0], acc[sw][j][0]);
-                            acc[sw][j][1] = fmaf(s0, P[sw][j][1], acc[sw][j][1]);
-                            acc[sw][j][2] = fmaf(s1, P[sw][j][2], acc[sw][j][2]);
-                            acc[sw][j][3] = fmaf(s1, P[sw][j][3], acc[sw][j][3]);
+                            if (FULL && gl == 0) {
+                                accc[sw][j][0] = s0 * P[sw][j][0];
+                                accc[sw][j][1] = s0 * P[sw][j][1];
+                                accc[sw][j][2] = s1 * P[sw][j][2];
+                                accc[sw][j][3] = s1 * P[sw][j][3];
+                            } else {
+                                accc[sw][j][0] = fmaf(s0, P[sw][j][0], accc[sw][j][0]);
+                                accc[sw][j][1] = fmaf(s0, P[sw][j][1], accc[sw][j][1]);
+                                accc[sw][j][2] = fmaf(s1, P[sw][j][2], accc[sw][j][2]);
+                                accc[sw][j][3] = fmaf(s1, P[sw][j][3], accc[sw][j][3]);
+                            }
                         }
                     }
                 }
@@ -549,8 +603,20 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                 groups(std::true_type{});
             else
                 groups(std::false_type{});
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const float2 rf = *reinterpret_cast<const float2*>(xrf + 8 * j + 2 * t);
+#pragma unroll
+                for (int sw = 0; sw < kSPW; ++sw) {
+                    if (!act[sw]) continue;
+                    acc[sw][j][0] = fmaf(rf.x, accc[sw][j][0], acc[sw][j][0]);
+                    acc[sw][j][1] = fmaf(rf.y, accc[sw][j][1], acc[sw][j][1]);
+                    acc[sw][j][2] = fmaf(rf.x, accc[sw][j][2], acc[sw][j][2]);
+                    acc[sw][j][3] = fmaf(rf.y, accc[sw][j][3], acc[sw][j][3]);
+                }
+            }
 
-            // bias and offset terms of the chunk, (b | s) x (XS | -OFF*XS) / sigma:
+            // bias and offset terms of the chunk, (b | s) x (XS | -XSc) / sigma:
             // K half kh takes slab kh of its pair
 #pragma unroll
             for (int sw = 0; sw < kSPW; ++sw) {
@@ -640,13 +706,15 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
 __global__ void __launch_bounds__(kReduceThreads) qmm_splitk_reduce_kernel(const __grid_constant__ ReduceParams p);
 
 // ---------------------------------------------------------------------------
-// Diagnostic unpack: one thread per (row, virtual block, lane position t).
+// Diagnostic unpack: one thread per (row, k32 block, lane position t). Runs the
+// main kernel's unpacker and reads each code back out of its binary16 value
+// 1024 + q * 2^j (0xFF where the pattern is not of that form).
 // ---------------------------------------------------------------------------
 template <int BITS>
 __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restrict__ w, int64_t K, int64_t N,
                                                          uint8_t* __restrict__ codes) {
     constexpr int BB = vblock_bytes(BITS);
-    const int64_t vbk = (BITS == 8) ? K / 16 : K / 32;          // virtual blocks per row
+    const int64_t vbk = K / 32;                                  // k32 blocks per row
     const int64_t total = N * vbk * 4;
     const int64_t row_bytes = K * BITS / 8;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
@@ -658,29 +726,16 @@ __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restr
         const uint32_t* blk = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(w) + n * row_bytes + vb * BB);
         uint32_t r[4];
         unpack_block<BITS>(blk, t, r);
-        auto val = [](uint32_t reg, int hi) -> int {
-            const uint32_t h = (reg >> (16 * hi)) & 0xFFFFu;
-            return ((h & 0xFF80u) == 0x4300u) ? static_cast<int>(h & 0x7Fu) : -1;
-        };
-        uint8_t* out = codes + n * K;
-        if constexpr (BITS == 8) {
-            const int64_t kb = vb * 16 + 4 * t;
-            const int l0 = val(r[0], 0), l2 = val(r[0], 1), h0 = val(r[1], 0), h2 = val(r[1], 1);
-            const int l1 = val(r[2], 0), l3 = val(r[2], 1), h1 = val(r[3], 0), h3 = val(r[3], 1);
-            auto comb = [](int lo, int hi) -> uint8_t {
-                return (lo < 0 || hi < 0 || lo > 15 || hi > 15) ? 0xFF : static_cast<uint8_t>(lo + 16 * hi);
-            };
-            out[kb + 0] = comb(l0, h0);
-            out[kb + 1] = comb(l1, h1);
-            out[kb + 2] = comb(l2, h2);
-            out[kb + 3] = comb(l3, h3);
-        } else {
-            const int64_t kb = vb * 32 + 8 * t;
+        uint8_t* out = codes + n * K + vb * 32 + 8 * t;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int lo = val(r[q], 0), hi = val(r[q], 1);
-                out[kb + q] = lo < 0 ? 0xFF : static_cast<uint8_t>(lo);
-                out[kb + q + 4] = hi < 0 ? 0xFF : static_cast<uint8_t>(hi);
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t v = (r[q] >> (16 * h)) & 0xFFFFu;
+                const int j = slot_shift(BITS, q, h);
+                const uint32_t mant = v & 0x3FFu;
+                const bool okv = (v & 0xFC00u) == 0x6400u && (mant & ((1u << j) - 1u)) == 0 && (mant >> j) < (1u << BITS);
+                out[slot_code(BITS, q, h)] = okv ? static_cast<uint8_t>(mant >> j) : static_cast<uint8_t>(0xFF);
             }
         }
     }

@@ -14,11 +14,10 @@
 //     fixed order through a small shared-memory scratch at the end of the row
 //     block.
 //   * Inside a slab the contraction runs on tensor cores with
-//     mma.m16n8k16: A = 16 weight rows x 16 codes (unpacked to bf16 128 + q),
-//     B = 16 codes x 8 activation rows, fp32 accumulators. One "virtual k32
-//     block" feeds two such MMAs. 8-bit codes are split into their two nibbles
-//     (weights 1 and 16), so an 8-bit k32 block of real codes is two virtual
-//     blocks.
+//     mma.m16n8k16: A = 16 weight rows x 16 codes (unpacked to the exact
+//     binary16 values 1024 + q * 2^j), B = 16 codes x 8 activation rows (x
+//     times a power-of-two range factor, times 2^-j, in binary16), fp32
+//     accumulators. One k32 block of codes feeds two such MMAs.
 #pragma once
 
 #include <stdint.h>
@@ -46,15 +45,13 @@ constexpr int kReduceThreads = 256;
 
 QMM_HD constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// Virtual k32 blocks per scale group (an 8-bit code counts as two nibbles).
-QMM_HD constexpr int vblocks_per_group(int bits, int group) {
-    return (group / 32) * (bits == 8 ? 2 : 1);
-}
+// k32 blocks per scale group.
+QMM_HD constexpr int vblocks_per_group(int bits, int group) { return (void)bits, group / 32; }
 QMM_HD constexpr int vblocks_per_chunk(int bits, int group) {
     return kGPC * vblocks_per_group(bits, group);
 }
-// Bytes of one weight row that one virtual block consumes.
-QMM_HD constexpr int vblock_bytes(int bits) { return bits == 8 ? 16 : 4 * bits; }
+// Bytes of one weight row that one k32 block consumes.
+QMM_HD constexpr int vblock_bytes(int bits) { return 4 * bits; }
 // Packed bytes of one weight row in a full chunk.
 QMM_HD constexpr int chunk_row_bytes(int bits, int group) { return kGPC * group * bits / 8; }
 // The weight tile of a stage arrives as TMA boxes of kTN rows x W bytes, W the
@@ -68,15 +65,15 @@ QMM_HD constexpr int wbox_count(int bits, int group) { return chunk_row_bytes(bi
 QMM_HD constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 
 // Staged activations, per chunk: MMA B fragments (one 16-byte vector per lane
-// per virtual block per 8-row tile), the bias-term fragments, and one scale
-// factor per activation row.
+// per k32 block per 8-row tile), the bias-term fragments, and two factors per
+// activation row (the bias-term range factor and 1/f, f the x range factor).
 QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
 QMM_HD constexpr int xprep_frag_bytes(int bits, int group, int mb) {
     return vblocks_per_chunk(bits, group) * n8_tiles(mb) * 512;
 }
 QMM_HD constexpr int xprep_bias_bytes(int mb) { return n8_tiles(mb) * 512; }
 QMM_HD constexpr int xprep_chunk_bytes(int bits, int group, int mb) {
-    return round_up(xprep_frag_bytes(bits, group, mb) + xprep_bias_bytes(mb) + mb * 4, 128);
+    return round_up(xprep_frag_bytes(bits, group, mb) + xprep_bias_bytes(mb) + 2 * mb * 4, 128);
 }
 
 // One pipeline stage in shared memory (1024-byte aligned: the swizzle atom).
@@ -94,8 +91,5 @@ QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int stages) {
     return 1024 + stages * stage_bytes(bits, group, mb) + stages * 16 + reduce_scratch_bytes(mb);
 }
 
-// Offset the unpacked codes carry (128 per bf16 slot; an 8-bit code is
-// 16*(128+hi) + (128+lo) over its two slots = q + 2176).
-QMM_HD constexpr float code_offset(int bits) { return bits == 8 ? 2176.0f : 128.0f; }
 
 }  // namespace qmmk

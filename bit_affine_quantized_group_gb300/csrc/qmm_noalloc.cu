@@ -204,7 +204,7 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     h.out_mode = out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16;
     h.sb_tma = (G % 8 == 0) ? 1 : 0;
     h.sb_vec16 = h.sb_tma;
-    h.unpack_magic = kBf16x2_128;
+    h.unpack_magic = kF16x2_1024;
     h.banks = 1;
     h.xprep_bytes = static_cast<int64_t>(xprep_bytes);
     h.rows_total = N;

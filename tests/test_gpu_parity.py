@@ -175,6 +175,34 @@ def test_row_independence(q, oracle_mod):
     assert all(bitwise[:1]), bitwise
 
 
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+def test_activation_dynamic_range(q, oracle_mod, bits):
+    """Rows of x at very different magnitudes (2^-110 .. 2^100), a row whose
+    groups alternate between 2^30 and 2^-30, a zero row and a zero chunk. The
+    activations enter the tensor cores as binary16 under a power-of-two range
+    factor per (row, 8-group chunk); each row must stay within tolerance of its
+    own largest output (a row of zeros gives exact zeros)."""
+    from tests._helpers import check_f32
+    K, N, group = 1024, 200, 32          # 4 chunks
+    inp = datagen.gen_qmm(77 + bits, 16, K, N, bits, group)
+    xf = (inp.x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for m, e in enumerate([-110, -80, -40, -10, 0, 10, 40, 80, 100]):
+        xf[m] *= 2.0 ** e
+    xf[9] *= np.where((np.arange(K) // group) % 2 == 0, 2.0 ** 30, 2.0 ** -30)
+    xf[10] = 0.0
+    xf[11, 256:512] = 0.0
+    inp.x = datagen.f64_to_bf16_bits(xf)
+    y_ref = oracle_mod.qmm_f64(inp.x, inp.words[0], inp.scales[0], inp.biases[0], K, N, bits, group)
+    plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="f32", splits=1)
+    x, w, s, b = dev_tensors(inp)
+    y = to_f64(run_forward(plan, x, w, s, b, 16))
+    assert np.all(np.isfinite(y))
+    for m in range(16):
+        check_f32(y[m:m + 1], y_ref[m:m + 1])
+    assert np.all(y[10] == 0.0)
+    assert plan.error_flags() == 0
+
+
 def test_banked_equals_single(q):
     import torch
     K, N, bits, group, B = 1024, 700, 4, 64, 5

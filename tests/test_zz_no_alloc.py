@@ -32,8 +32,8 @@ def _call(q, x, M, w, s, b, K, N, bits, group, out_dtype, out):
 
 
 def test_noalloc_rejects_oversized_staging_before_touching_the_device(q):
-    # 8-bit codes, groups of 64, 16 rows: the largest K that fits is 62976
-    K, N, bits, group = 65536, 64, 8, 64
+    # 8-bit codes, groups of 64, 16 rows: the largest K that fits is 122368
+    K, N, bits, group = 131072, 64, 8, 64
     st = _call(q, 0x1000, 16, 0x2000, 0x3000, 0x4000, K, N, bits, group, q.QMM_OUT_BF16, 0x5000)
     assert st == q.QMM_ERR_SCRATCH_LIMIT
     assert "scratch" in q.status_string(st)
