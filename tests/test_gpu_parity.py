@@ -157,22 +157,27 @@ def test_deterministic(q, splits):
         assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
-def test_row_independence(q, oracle_mod):
-    """Row m of an M-row call vs the 1-row call on the same x row: within
-    tolerance always; bitwise equality is reported in the assertion message."""
-    K, N, bits, group = 2048, 512, 4, 32
-    inp = datagen.gen_qmm(5, 16, K, N, bits, group)
-    plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="f32", splits=1)
+@pytest.mark.parametrize("bits,group,splits", [(4, 32, 1), (6, 64, 2), (8, 32, 3), (5, 32, 1)])
+def test_row_independence(q, oracle_mod, bits, group, splits):
+    """Row m of an M-row call equals the 1-row call on the same x row bitwise, for
+    every m and M in {16, 9, 5} (8- and 16-row tiles): each activation row is an
+    independent MMA column whose range factors depend on that row alone, and the
+    split count is a property of the plan, not of M."""
+    K, N = 2048, 512
+    inp = datagen.gen_qmm(5 + bits, 16, K, N, bits, group)
+    plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="f32", splits=splits)
     x, w, s, b = dev_tensors(inp)
-    y16 = to_f64(run_forward(plan, x, w, s, b, 16))
     y_ref = oracle_mod.qmm_f64(inp.x, inp.words[0], inp.scales[0], inp.biases[0], K, N, bits, group)
-    bitwise = []
+    ys = {M: to_f64(run_forward(plan, x, w, s, b, M)) for M in (16, 9, 5)}
+    mismatched = []
     for m in range(16):
         y1 = to_f64(run_forward(plan, x[m:m + 1].contiguous(), w, s, b, 1))
         check(y1[0][None], y_ref[m][None], "f32")
-        bitwise.append(bool(np.array_equal(y1[0], y16[m])))
-    # rows 0..7 run identical arithmetic in both calls (8-row tile); report the rest
-    assert all(bitwise[:1]), bitwise
+        for M, yM in ys.items():
+            if m < M and not np.array_equal(y1[0], yM[m]):
+                mismatched.append((M, m))
+    assert not mismatched, mismatched
+    assert plan.error_flags() == 0
 
 
 @pytest.mark.parametrize("bits", [4, 5, 6, 8])
