@@ -82,6 +82,8 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 cudaError_t configure(int bits, int group, int mb, int smem) {
     switch (bits) {
+        case 2: return configure_kernels<2>(group, mb, smem);
+        case 3: return configure_kernels<3>(group, mb, smem);
         case 4: return configure_kernels<4>(group, mb, smem);
         case 5: return configure_kernels<5>(group, mb, smem);
         case 6: return configure_kernels<6>(group, mb, smem);
@@ -93,6 +95,8 @@ cudaError_t configure(int bits, int group, int mb, int smem) {
 cudaError_t launch(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,
                    const MainParams<kMaxBanks>* banked) {
     switch (bits) {
+        case 2: return launch_forward<2>(group, L, single, banked);
+        case 3: return launch_forward<3>(group, L, single, banked);
         case 4: return launch_forward<4>(group, L, single, banked);
         case 5: return launch_forward<5>(group, L, single, banked);
         case 6: return launch_forward<6>(group, L, single, banked);
@@ -188,7 +192,7 @@ int qmm_validate_desc(const qmm_desc* d) {
     if (d->out_dtype != QMM_OUT_F32 && d->out_dtype != QMM_OUT_BF16) return QMM_ERR_INVALID_ARG;
     if (d->splits < 0 || d->splits > QMM_MAX_SPLITS) return QMM_ERR_INVALID_ARG;
     if (d->max_banks < 1 || d->max_banks > QMM_MAX_BANKS) return QMM_ERR_INVALID_ARG;
-    if (d->bits != 4 && d->bits != 5 && d->bits != 6 && d->bits != 8) return QMM_ERR_UNSUPPORTED;
+    if (d->bits < 2 || d->bits > 8 || d->bits == 7) return QMM_ERR_UNSUPPORTED;
     if (d->group != 32 && d->group != 64) return QMM_ERR_UNSUPPORTED;
     if ((d->K * d->bits) % 128 != 0) return QMM_ERR_UNSUPPORTED;
     if ((d->K / d->group) % 2 != 0) return QMM_ERR_UNSUPPORTED;
@@ -408,13 +412,15 @@ int qmm_forward(const qmm_plan_t* p, const void* x_bf16, int M, const uint32_t* 
 }
 
 int qmm_unpack_codes(const uint32_t* packed_w, int64_t K, int64_t N, int bits, uint8_t* codes, void* stream) {
-    if (bits != 4 && bits != 5 && bits != 6 && bits != 8) return QMM_ERR_UNSUPPORTED;
+    if (bits < 2 || bits > 8 || bits == 7) return QMM_ERR_UNSUPPORTED;
     if (K <= 0 || N < 0 || K % 32 != 0 || K > (1LL << 24)) return QMM_ERR_INVALID_ARG;
     if (N == 0) return QMM_OK;
     if (packed_w == nullptr || codes == nullptr || !aligned(packed_w, 4)) return QMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (bits) {
+        case 2: e = launch_unpack<2>(packed_w, K, N, codes, st); break;
+        case 3: e = launch_unpack<3>(packed_w, K, N, codes, st); break;
         case 4: e = launch_unpack<4>(packed_w, K, N, codes, st); break;
         case 5: e = launch_unpack<5>(packed_w, K, N, codes, st); break;
         case 6: e = launch_unpack<6>(packed_w, K, N, codes, st); break;

@@ -180,20 +180,26 @@ constexpr uint32_t kF16x2_1024 = 0x64006400u;
 
 // Slot tables: which of the lane's 8 codes, and its mantissa shift j.
 QMM_HD constexpr int slot_code(int bits, int r, int h) {
-    return bits == 4 ? (h == 0 ? r : r + 4)
+    return bits == 2 ? r + 4 * h
+         : bits == 3 ? (r < 3 ? (h == 0 ? r : r + 5) : 3 + h)
+         : bits == 4 ? (h == 0 ? r : r + 4)
          : bits == 8 ? ((r >> 1) * 4 + (r & 1) + 2 * h)
          : bits == 5 ? (h == 0 ? r : r + 4)
          : /* 6 */     (r < 3 ? (h == 0 ? r : r + 3) : 6 + h);
 }
 QMM_HD constexpr int slot_shift(int bits, int r, int h) {
-    return bits == 4 ? ((r & 1) ? 4 : 0)
+    return bits == 2 ? 2 * r
+         : bits == 3 ? ((r < 3 && h == 0) ? 1 : 0)
+         : bits == 4 ? ((r & 1) ? 4 : 0)
          : bits == 8 ? 0
          : bits == 5 ? (h == 0 ? 0 : 4)
          : /* 6 */     ((r < 3 && h == 1) ? 2 : 0);
 }
 // Shift j of the lane's code i (the inverse view of the tables).
 QMM_HD constexpr int code_shift(int bits, int i) {
-    return bits == 4 ? ((i & 1) ? 4 : 0)
+    return bits == 2 ? 2 * (i & 3)
+         : bits == 3 ? (i < 3 ? 1 : 0)
+         : bits == 4 ? ((i & 1) ? 4 : 0)
          : bits == 8 ? 0
          : bits == 5 ? (i < 4 ? 0 : 4)
          : /* 6 */     ((i >= 3 && i <= 5) ? 2 : 0);
@@ -217,14 +223,37 @@ __device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t (&r)[
     r[3] = ((w1 >> 8) & 0x00FF00FFu) | magic;  // c5, c7
 }
 
-// 5- or 6-bit: the lane's 8 codes are 5 or 6 bytes starting at byte BITS*t of
-// the block; `lo`, `hi` are the two words covering them and `sh` (0, 8, 16,
-// 24) the bit offset of the first code inside `lo`.
+// 2-bit: the lane's 8 codes are the 16 bits at bit 16 * (t & 1) of word w.
+// `sel` is the byte-permute selector that moves those two bytes to bytes 0
+// and 2 (0x4140 for t even, 0x4342 for t odd; selector 4 picks a zero byte),
+// after which code q sits at bit 2q of the low half and code q + 4 at bit 2q
+// of the high half.
+__device__ __forceinline__ void unpack2(uint32_t w, uint32_t sel, uint32_t (&r)[4], uint32_t magic = kF16x2_1024) {
+    const uint32_t y = __byte_perm(w, 0u, sel);
+    r[0] = (y & 0x00030003u) | magic;          // c0, c4   (shift 0)
+    r[1] = (y & 0x000C000Cu) | magic;          // c1, c5   (shift 2)
+    r[2] = (y & 0x00300030u) | magic;          // c2, c6   (shift 4)
+    r[3] = (y & 0x00C000C0u) | magic;          // c3, c7   (shift 6)
+}
+QMM_HD constexpr uint32_t unpack2_selector(int t) { return (t & 1) ? 0x4342u : 0x4140u; }
+
+// 3-, 5- or 6-bit: the lane's 8 codes are 3, 5 or 6 bytes starting at byte
+// BITS*t of the block; `lo`, `hi` are the two words covering them and `sh`
+// (0, 8, 16, 24) the bit offset of the first code inside `lo`.
 template <int BITS>
 __device__ __forceinline__ void unpack_odd(uint32_t lo, uint32_t hi, uint32_t sh, uint32_t (&r)[4],
                                            uint32_t magic = kF16x2_1024) {
     const uint64_t v = ((static_cast<uint64_t>(hi) << 32) | lo) >> sh;
-    if constexpr (BITS == 5) {
+    if constexpr (BITS == 3) {
+        // the 24 code bits sit in the low word: c_i at bit 3i. (c_i, c_{i+5}) are
+        // 15 bits apart, so one left shift by 1 puts c_i at bit 1 and c_{i+5} at
+        // bit 16 (shifts 1 and 0); c3 and c4 take a shift each.
+        const uint32_t u = static_cast<uint32_t>(v);
+        r[0] = ((u << 1) & 0x0007000Eu) | magic;               // c0 (shift 1), c5
+        r[1] = ((u >> 2) & 0x0007000Eu) | magic;               // c1 (shift 1), c6
+        r[2] = ((u >> 5) & 0x0007000Eu) | magic;               // c2 (shift 1), c7
+        r[3] = ((u >> 9) & 0x7u) | ((u << 4) & 0x00070000u) | magic;   // c3, c4
+    } else if constexpr (BITS == 5) {
         // c_i at bit 0 and c_{i+4} at bit 20 (= 16 + 4) of the same window
 #pragma unroll
         for (int i = 0; i < 4; ++i) r[i] = (static_cast<uint32_t>(v >> (5 * i)) & 0x01F0001Fu) | magic;
@@ -246,13 +275,17 @@ __device__ __forceinline__ uint32_t odd_shift(int t) { return static_cast<uint32
 // 8-byte aligned for 8-bit codes). Used by the unpack diagnostic.
 template <int BITS>
 __device__ __forceinline__ void unpack_block(const uint32_t* blk, int t, uint32_t (&r)[4]) {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+        unpack2(blk[t >> 1], unpack2_selector(t), r);
+    } else if constexpr (BITS == 4) {
         unpack4(blk[t], r);
     } else if constexpr (BITS == 8) {
         unpack8(blk[2 * t], blk[2 * t + 1], r);
     } else {
+        // a block holds BITS words; the next word is read only when it is still
+        // inside the block (3-bit lane 3 fits in its first word)
         const int w = odd_word<BITS>(t);
-        unpack_odd<BITS>(blk[w], blk[w + 1], odd_shift<BITS>(t), r);
+        unpack_odd<BITS>(blk[w], w + 1 < BITS ? blk[w + 1] : 0u, odd_shift<BITS>(t), r);
     }
 }
 

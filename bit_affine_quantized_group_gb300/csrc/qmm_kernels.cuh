@@ -451,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     const uint32_t magic = p.unpack_magic;
     const int g = lane >> 2;
     const int t = lane & 3;
+    const uint32_t sel2 = unpack2_selector(t);   // 2-bit codes only
     const int sp = warp % kSlabPairs;        // slabs sp and sp + 4
     const int kh = warp / kSlabPairs;        // chunk groups 4*kh .. 4*kh + 3
     const int gbase = kh * kGroupsPerWarp;
@@ -555,6 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                                 const uint2 u1 = *reinterpret_cast<const uint2*>(a0 + (g + 8) * W);
                                 unpack8(u0.x, u0.y, ra, magic);
                                 unpack8(u1.x, u1.y, rb, magic);
+                            } else if constexpr (BITS == 2) {
+                                // lane t's 8 codes are half of word t / 2 of the block
+                                const int b0 = vb * BB + 4 * odd_word<BITS>(t);
+                                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(row0[sw], b0));
+                                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(row0[sw] + 8, b0));
+                                unpack2(w0, sel2, ra, magic);
+                                unpack2(w1, sel2, rb, magic);
                             } else {
                                 const int b0 = vb * BB + 4 * odd_word<BITS>(t);
                                 const int r0 = row0[sw], r1 = row0[sw] + 8;

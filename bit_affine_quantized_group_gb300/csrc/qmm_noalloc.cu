@@ -51,10 +51,12 @@ struct DeviceSetup {
 DeviceSetup g_dev[kMaxDevices];
 std::mutex g_mutex;
 
-int bits_index(int bits) { return bits == 4 ? 0 : bits == 5 ? 1 : bits == 6 ? 2 : 3; }
+int bits_index(int bits) { return bits == 2 ? 4 : bits == 3 ? 5 : bits == 4 ? 0 : bits == 5 ? 1 : bits == 6 ? 2 : 3; }
 
 cudaError_t configure_format(int bits, int group, int mb, int smem) {
     switch (bits) {
+        case 2: return configure_kernels<2>(group, mb, smem);
+        case 3: return configure_kernels<3>(group, mb, smem);
         case 4: return configure_kernels<4>(group, mb, smem);
         case 5: return configure_kernels<5>(group, mb, smem);
         case 6: return configure_kernels<6>(group, mb, smem);
@@ -64,6 +66,8 @@ cudaError_t configure_format(int bits, int group, int mb, int smem) {
 
 cudaError_t launch_format(int bits, int group, const LaunchCfg& L, const MainParams<1>* mp) {
     switch (bits) {
+        case 2: return launch_forward<2>(group, L, mp, nullptr);
+        case 3: return launch_forward<3>(group, L, mp, nullptr);
         case 4: return launch_forward<4>(group, L, mp, nullptr);
         case 5: return launch_forward<5>(group, L, mp, nullptr);
         case 6: return launch_forward<6>(group, L, mp, nullptr);

@@ -25,7 +25,10 @@
  *   out     [M, N]          float32 or bfloat16 (round to nearest even),
  *                           overwritten (never accumulated into).
  *
- * Supported formats: bits in {4, 5, 6, 8}, group in {32, 64}, 1 <= M <= 16.
+ * Supported formats: bits in {2, 3, 4, 5, 6, 8}, group in {32, 64}, 1 <= M <= 16.
+ * (2-bit tensors are in use beside 4/8-bit ones per "Qwen3.8 Flash Next
+ * performance and parity receipt", MTPLX logic review, and the "JANGH split-K
+ * verify tile" commit tests 2/4/8-bit codes; 3-bit follows the same stream.)
  * Requirements checked before any launch: K % group == 0; K*bits % 128 == 0
  * (every packed row starts on a 16-byte boundary); K/group even; packed
  * weights, scales and biases 16-byte aligned device pointers; x and out
@@ -84,7 +87,7 @@ enum { QMM_OUT_F32 = 0, QMM_OUT_BF16 = 1 };
 typedef struct qmm_desc {
     int64_t K;          /* reduction length (codes per weight row) */
     int64_t N;          /* output columns (weight rows) */
-    int32_t bits;       /* code width: 4, 5, 6 or 8 */
+    int32_t bits;       /* code width: 2, 3, 4, 5, 6 or 8 */
     int32_t group;      /* codes per scale/bias group: 32 or 64 */
     int32_t max_M;      /* largest M forward will be called with, 1..16 */
     int32_t out_dtype;  /* QMM_OUT_F32 or QMM_OUT_BF16 */
@@ -175,8 +178,9 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
 /*
  * Diagnostic: run the main kernel's in-register code unpacking on packed
  * weights and write the decoded codes, codes[n*K + k] = q[n,k] (uint8, device
- * pointer, N*K bytes). A code whose unpacked bfloat16 image is not the exact
- * value 128 + q is written as 0xFF. Asynchronous on `stream`.
+ * pointer, N*K bytes). A code whose unpacked binary16 image is not the exact
+ * value 1024 + q * 2^j (j the code's mantissa shift) is written as 0xFF.
+ * Asynchronous on `stream`.
  */
 int qmm_unpack_codes(const uint32_t* packed_w, int64_t K, int64_t N, int bits, uint8_t* codes,
                      void* stream);

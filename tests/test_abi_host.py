@@ -48,7 +48,7 @@ GOOD = dict(K=5120, N=17408, bits=4, group=32, max_M=16, out_dtype="bf16", split
 @pytest.mark.parametrize("change,expect", [
     ({}, 0),
     ({"bits": 5}, 0), ({"bits": 6}, 0), ({"bits": 8}, 0), ({"group": 64}, 0),
-    ({"bits": 3}, 2), ({"bits": 2}, 2), ({"bits": 7}, 2), ({"group": 128}, 2), ({"group": 16}, 2),
+    ({"bits": 3}, 0), ({"bits": 2}, 0), ({"bits": 7}, 2), ({"bits": 1}, 2), ({"group": 128}, 2), ({"group": 16}, 2),
     ({"bits": 0}, 1), ({"K": 0}, 1), ({"N": 0}, 1), ({"K": 5120 + 16}, 1),
     ({"max_M": 0}, 1), ({"max_M": 17}, 1), ({"splits": -1}, 1), ({"splits": 17}, 1),
     ({"max_banks": 0}, 1), ({"max_banks": 65}, 1),
@@ -83,7 +83,7 @@ def test_workspace_bytes(q):
     assert 0 < n1 < 1024 * 1024
     # splits = 0 (automatic) is sized for the largest automatic choice (here 20 chunks / 3 = 6)
     assert n >= n1 + 6 * 16 * 17408 * 4
-    bad = q.make_desc(**{**GOOD, "bits": 3})
+    bad = q.make_desc(**{**GOOD, "bits": 7})
     assert q.workspace_bytes(bad) == 0
     # explicit slices need fp32 partials for max_banks * splits * max_M * N
     d2 = q.make_desc(K=17408, N=5120, bits=4, group=64, max_M=16, out_dtype="bf16", splits=8, max_banks=1)
@@ -148,7 +148,7 @@ def test_null_plan_and_handles(q):
     lib.qmm_destroy(None)   # accepted
     # invalid descriptors are rejected before any device query
     out = ctypes.c_void_p(1)
-    bad = q.make_desc(**{**GOOD, "bits": 3})
+    bad = q.make_desc(**{**GOOD, "bits": 7})
     assert lib.qmm_plan(ctypes.byref(out), ctypes.byref(bad), None, 0) == q.QMM_ERR_UNSUPPORTED
     assert out.value is None
     assert lib.qmm_plan(None, ctypes.byref(bad), None, 0) == q.QMM_ERR_INVALID_ARG
@@ -156,7 +156,7 @@ def test_null_plan_and_handles(q):
 
 def test_unpack_codes_argument_errors(q):
     lib = q.lib
-    assert lib.qmm_unpack_codes(None, 64, 1, 3, None, None) == q.QMM_ERR_UNSUPPORTED
+    assert lib.qmm_unpack_codes(None, 64, 1, 7, None, None) == q.QMM_ERR_UNSUPPORTED
     assert lib.qmm_unpack_codes(None, 48, 1, 4, None, None) == q.QMM_ERR_INVALID_ARG
     assert lib.qmm_unpack_codes(None, 64, 1, 4, None, None) == q.QMM_ERR_INVALID_ARG
     assert lib.qmm_unpack_codes(None, 64, 0, 4, None, None) == q.QMM_OK

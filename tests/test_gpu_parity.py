@@ -44,7 +44,7 @@ def _K_for(bits, group, G):
 # ---------------------------------------------------------------------------
 # Unpack: bit-exact against the oracle's bit-at-a-time decoder
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 @pytest.mark.parametrize("K,N", [(256, 37), (2048, 9)])
 def test_unpack_bit_exact(q, oracle_mod, bits, K, N):
     import torch
@@ -57,7 +57,7 @@ def test_unpack_bit_exact(q, oracle_mod, bits, K, N):
     assert np.array_equal(codes.cpu().numpy(), ref)
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 def test_unpack_every_value_every_offset(q, oracle_mod, bits):
     """Rows where position k holds (v + 7k) mod 2^bits: every value at every offset."""
     import torch
@@ -73,7 +73,7 @@ def test_unpack_every_value_every_offset(q, oracle_mod, bits):
 # ---------------------------------------------------------------------------
 # Small-shape parity over formats x rows x output x slices
 # ---------------------------------------------------------------------------
-FORMATS = [(4, 32), (4, 64), (5, 32), (5, 64), (6, 32), (6, 64), (8, 32), (8, 64)]
+FORMATS = [(2, 32), (2, 64), (3, 32), (3, 64), (4, 32), (4, 64), (5, 32), (5, 64), (6, 32), (6, 64), (8, 32), (8, 64)]
 MS = [1, 2, 3, 5, 8, 9, 12, 16]
 
 
@@ -96,7 +96,7 @@ def test_small_parity(q, oracle_mod, bits, group, out_dtype, splits):
     assert plan.error_flags() == 0
 
 
-@pytest.mark.parametrize("bits,group,G", [(4, 32, 10), (4, 64, 6), (6, 32, 14), (8, 64, 2), (5, 32, 12)])
+@pytest.mark.parametrize("bits,group,G", [(4, 32, 10), (4, 64, 6), (6, 32, 14), (8, 64, 2), (5, 32, 12), (2, 64, 6), (3, 32, 12)])
 @pytest.mark.parametrize("N", [1, 15, 17, 129, 1000])
 def test_ragged_shapes(q, oracle_mod, bits, group, G, N):
     """K/group not a multiple of 8 (4-byte scale rows, partial chunks) and tiny/ragged N."""
@@ -157,7 +157,7 @@ def test_deterministic(q, splits):
         assert all(torch.equal(outs[0], o) for o in outs[1:])
 
 
-@pytest.mark.parametrize("bits,group,splits", [(4, 32, 1), (6, 64, 2), (8, 32, 3), (5, 32, 1)])
+@pytest.mark.parametrize("bits,group,splits", [(4, 32, 1), (6, 64, 2), (8, 32, 3), (5, 32, 1), (2, 32, 2), (3, 64, 1)])
 def test_row_independence(q, oracle_mod, bits, group, splits):
     """Row m of an M-row call equals the 1-row call on the same x row bitwise, for
     every m and M in {16, 9, 5} (8- and 16-row tiles): each activation row is an
@@ -180,7 +180,7 @@ def test_row_independence(q, oracle_mod, bits, group, splits):
     assert plan.error_flags() == 0
 
 
-@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 def test_activation_dynamic_range(q, oracle_mod, bits):
     """Rows of x at very different magnitudes (2^-110 .. 2^100), a row whose
     groups alternate between 2^30 and 2^-30, a zero row and a zero chunk. The

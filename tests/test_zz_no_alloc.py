@@ -40,7 +40,7 @@ def test_noalloc_rejects_oversized_staging_before_touching_the_device(q):
     # ordinary argument errors are reported the same way as qmm_forward's
     assert _call(q, 0, 4, 0x2000, 0x3000, 0x4000, 2048, 64, 4, 64, q.QMM_OUT_F32, 0x5000) == q.QMM_ERR_INVALID_ARG
     assert _call(q, 0x1000, 17, 0x2000, 0x3000, 0x4000, 2048, 64, 4, 64, q.QMM_OUT_F32, 0x5000) == q.QMM_ERR_INVALID_ARG
-    assert _call(q, 0x1000, 4, 0x2000, 0x3000, 0x4000, 2048, 64, 3, 64, q.QMM_OUT_F32, 0x5000) == q.QMM_ERR_UNSUPPORTED
+    assert _call(q, 0x1000, 4, 0x2000, 0x3000, 0x4000, 2048, 64, 7, 64, q.QMM_OUT_F32, 0x5000) == q.QMM_ERR_UNSUPPORTED
 
 
 @pytest.mark.gpu
