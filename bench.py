@@ -440,6 +440,72 @@ def run_ncu_case(args):
     print(f"ncu case ok: {args.case_workload} M={M} bits={bits} splits={plan.info()['splits']} calls={args.calls}")
 
 
+COST_TABLE_CASES = [("mlp_up", 4), ("down_longk", 4), ("mixed_widths", 5), ("mixed_widths", 6),
+                    ("mixed_widths", 8), ("lm_head", 8)]
+
+
+def run_cost_table(args):
+    """Per-M cost table (us/call for every M in 1..16) of the named workloads,
+    for a row-width chooser: CUDA-graph replay over enough rotating weight
+    copies to exceed 3x L2 (device clones of one generated copy), one JSON line."""
+    import torch
+    from bit_affine_quantized_group_gb300 import _build
+    _build.build()
+    import bit_affine_quantized_group_gb300 as q
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    table = {}
+    for name, bits in COST_TABLE_CASES:
+        wl = datagen.WORKLOADS[name]
+        K, N, group = wl["K"], wl["N"], wl["group"]
+        inp = datagen.gen_qmm(datagen.workload_seed(name) + bits, 16, K, N, bits, group)
+        x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        w0 = torch.from_numpy(inp.words[0].view(np.int32)).to(dev)
+        s0 = torch.from_numpy(inp.scales[0].view(np.int16)).to(dev).view(torch.float16)
+        b0 = torch.from_numpy(inp.biases[0].view(np.int16)).to(dev).view(torch.float16)
+        del inp
+        per_copy = algorithmic_bytes(16, K, N, bits, group, 2)
+        copies = max(1, -(-3 * 129 * 2 ** 20 // per_copy))
+        W = [w0] + [w0.clone() for _ in range(copies - 1)]
+        S = [s0] + [s0.clone() for _ in range(copies - 1)]
+        B = [b0] + [b0.clone() for _ in range(copies - 1)]
+        plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="bf16", splits=0, device=dev)
+        row = {}
+        for M in range(1, 17):
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+            def step():
+                for c in range(copies):
+                    q.forward(plan, x[:M], W[c], S[c], B[c], out, stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    step()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            reps = max(3, 400 // copies)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g.replay()
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+            row[str(M)] = {"us_per_call": round(us, 3),
+                           "gbs": round(algorithmic_bytes(M, K, N, bits, group, 2) / us / 1e3, 1)}
+            del g, out
+        assert plan.error_flags() == 0
+        table[f"{name}:{bits}-bit"] = {"K": K, "N": N, "group": group, "splits": plan.info()["splits"],
+                                       "copies": copies, "per_M": row}
+        del W, S, B, w0, s0, b0, plan
+        torch.cuda.empty_cache()
+    print(json.dumps({"cost_table": table, "unit": "us/call", "launch": "cuda_graph", "out": "bf16"}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -453,7 +519,12 @@ def main():
     ap.add_argument("--case-bits", type=int, default=0)
     ap.add_argument("--case-splits", type=int, default=0)
     ap.add_argument("--calls", type=int, default=5)
+    ap.add_argument("--cost-table", action="store_true",
+                    help="print the per-M (1..16) us/call table of the named workloads and exit")
     args = ap.parse_args()
+    if args.cost_table:
+        run_cost_table(args)
+        return
     if args.ncu_case:
         run_ncu_case(args)
         return

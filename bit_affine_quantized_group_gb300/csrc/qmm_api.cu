@@ -50,19 +50,44 @@ int chunks_of(const qmm_desc* d) {
 // Largest K-slice count a plan for d may use (the automatic choice never exceeds it).
 int splits_cap(const qmm_desc* d) {
     if (d->splits > 0) return d->splits;
-    int c = chunks_of(d) / 3;
+    int c = chunks_of(d) / 2;
     if (c < 1) c = 1;
     if (c > 8) c = 8;
     return c;
 }
 
-// Automatic K-slice count: enough (bank, slice, row) work for ~96 rows per SM,
-// at least 3 chunks per slice, at most 8 slices.
+// Automatic K-slice count from a per-CTA cost model, fitted on GB300 to the
+// 4-bit group-64 K=17408 N=5120 projection over 1, 2, 4 and 8 slices: a CTA
+// pays, per row block of up to 128 rows, one pass over its slice's chunks
+// (chunk bytes at about 28 GB/s per SM) plus about 2 us of restart, and
+// slicing adds about 3.7 us for the partial sums and their reduce. The work is
+// cut evenly over (bank, slice, row) space, so when the CTA count is not a
+// multiple of the bank-slice segments some CTA ranges straddle two segments
+// and pay one more row block. Slices keep at least 2 chunks.
 int auto_splits(const qmm_desc* d, int num_sms) {
     const int C = chunks_of(d);
-    int s = 1;
-    while (d->N * s < 96LL * num_sms && s < 8 && (s + 1) * 3 <= C) ++s;
-    return s;
+    const double chunk_us = kTN * (chunk_row_bytes(d->bits, d->group) + 4.0 * kGPC) / 28e3;
+    const double row_block_us = 2.0;
+    const double split_us = 3.7;
+    const int64_t banks = d->max_banks > 0 ? d->max_banks : 1;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int s = 1; s <= splits_cap(d); ++s) {
+        if (s > 1 && C / s < 2) break;
+        const int64_t rows_total = banks * s * d->N;
+        int64_t ctas = (rows_total + kSlab - 1) / kSlab;
+        if (ctas > num_sms) ctas = num_sms;
+        const int64_t rows_per_cta = (rows_total + ctas - 1) / ctas;
+        int64_t blocks = (rows_per_cta + kTN - 1) / kTN;
+        if (ctas % (banks * s) != 0) ++blocks;
+        const int per_slice = (C + s - 1) / s;
+        const double cost = blocks * (per_slice * chunk_us + row_block_us) + (s > 1 ? split_us : 0.0);
+        if (s == 1 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 int mb_index(int M) { return M > 8 ? 1 : 0; }

@@ -97,6 +97,10 @@ WORKLOADS = {
                          splits=[1], banks=1),
     "banked": dict(Ms=[1, 16], K=2048, N=8192, bits=[4], group=64, out="bf16", splits=[1],
                    banks=36),
+    # lm_head-class projection: 8-bit codes over a ~152k vocabulary (661 MB of
+    # codes, scales and biases streamed per call)
+    "lm_head": dict(Ms=[1, 8, 16], K=4096, N=151936, bits=[8], group=64, out="bf16", splits=[1],
+                    banks=1),
 }
 WORKLOAD_INDEX = {name: i for i, name in enumerate(WORKLOADS)}
 

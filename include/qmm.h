@@ -121,7 +121,7 @@ int qmm_validate_desc(const qmm_desc* d);
  * Device workspace a plan for `d` needs (bytes; 0 if d is invalid): the
  * per-call activation staging area plus split-K partials for
  * max_banks * splits * max_M * N floats (splits = 0 is sized for the largest
- * automatic choice, 8). Lets the caller (e.g. PyTorch's allocator) own it.
+ * automatic choice, min(8, chunks / 2) with chunks = ceil(K / group / 8)). Lets the caller (e.g. PyTorch's allocator) own it.
  */
 size_t qmm_workspace_bytes(const qmm_desc* d);
 

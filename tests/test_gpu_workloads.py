@@ -6,9 +6,12 @@ the launch configuration the benchmark uses (same plan settings):
   down_longk    M in {1,8,16}, K=17408, N=5120, 4-bit g64, splits {1,2,4,8}, bf16 out
   mixed_widths  M=8, K=5120, N=6144, bits {5,6,8}, g32, bf16 out
   banked        36 banks, M in {1,16}, K=2048, N=8192, 4-bit g64, bf16 out
+  lm_head       M in {1,8,16}, K=4096, N=151936, 8-bit g64, bf16 out
 
 Every output column is compared except in the banked workload, where two banks
-are compared in full and the others on 64 sampled columns each.
+are compared in full and the others on 64 sampled columns each, and in the
+lm_head workload, where 2304 columns (the first and last 128 and 2048 spread
+at random) are compared and every output is checked finite.
 """
 from __future__ import annotations
 
@@ -98,4 +101,21 @@ def test_banked(q, oracle_mod):
                 scale = max(float(np.max(np.abs(y_ref))), 1e-30)
                 bound = bf16_ulp(y_ref) + 1e-3 * scale
                 assert np.all(np.abs(y[:, cols] - y_ref) <= bound), f"bank {i}"
+    assert plan.error_flags() == 0
+
+
+def test_lm_head(q, oracle_mod):
+    wl = datagen.WORKLOADS["lm_head"]
+    K, N, group, bits = wl["K"], wl["N"], wl["group"], 8
+    inp = datagen.gen_qmm(datagen.workload_seed("lm_head"), 16, K, N, bits, group)
+    rng = np.random.default_rng(7)
+    cols = np.unique(np.concatenate([np.arange(128), np.arange(N - 128, N),
+                                     rng.choice(N, 2048, replace=False)])).astype(np.int64)
+    y_ref = oracle_mod.qmm_f64_cols(inp.x, inp.words[0], inp.scales[0], inp.biases[0], K, N, bits, group, cols)
+    x, w, s, b = dev_tensors(inp)
+    plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="bf16", splits=0)
+    for M in wl["Ms"]:
+        y = to_f64(run_forward(plan, x, w, s, b, M))
+        assert np.all(np.isfinite(y))
+        check(y[:, cols], y_ref[:M], "bf16")
     assert plan.error_flags() == 0
