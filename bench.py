@@ -22,6 +22,7 @@ import hashlib
 import json
 import os
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -114,7 +115,8 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw samples; the summary goes into the JSON line
+        self.path = os.path.join(tempfile.gettempdir(), f"qmm_bench_clocks_rank{gpu_index}_{os.getpid()}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
@@ -503,6 +505,58 @@ def run_cost_table(args):
                                        "copies": copies, "per_M": row}
         del W, S, B, w0, s0, b0, plan
         torch.cuda.empty_cache()
+    # fused gate/up (SwiGLU) on the mlp_up shape: one fused call against the two
+    # separate projections it replaces
+    wl = datagen.WORKLOADS["mlp_up"]
+    K, N, group, bits = wl["K"], wl["N"], wl["group"], 4
+    gi = datagen.gen_qmm(datagen.workload_seed("mlp_up"), 16, K, N, bits, group)
+    ui = datagen.gen_qmm(datagen.workload_seed("mlp_up") + 100, 16, K, N, bits, group)
+    x = torch.from_numpy(gi.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    dev_w = lambda a: (torch.from_numpy(a.words[0].view(np.int32)).to(dev),
+                       torch.from_numpy(a.scales[0].view(np.int16)).to(dev).view(torch.float16),
+                       torch.from_numpy(a.biases[0].view(np.int16)).to(dev).view(torch.float16))
+    g0, u0 = dev_w(gi), dev_w(ui)
+    del gi, ui
+    copies = 4
+    GS = [g0] + [tuple(t.clone() for t in g0) for _ in range(copies - 1)]
+    US = [u0] + [tuple(t.clone() for t in u0) for _ in range(copies - 1)]
+    plan = q.Plan(K, N, bits, group, max_M=16, out_dtype="bf16", splits=0, max_banks=2, device=dev)
+    fused_row = {}
+    for M in range(1, 17):
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        tmp = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        res = {}
+        for mode in ("fused", "separate"):
+            def step():
+                for c in range(copies):
+                    if mode == "fused":
+                        q.forward_swiglu(plan, x[:M], *GS[c], *US[c], out, stream=stream)
+                    else:
+                        q.forward(plan, x[:M], *GS[c], tmp, stream=stream)
+                        q.forward(plan, x[:M], *US[c], out, stream=stream)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    step()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step()
+            reps = 50
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g.replay()
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            res[mode] = e0.elapsed_time(e1) * 1e3 / (reps * copies)
+            del g
+        fused_row[str(M)] = {"fused_us": round(res["fused"], 3), "two_calls_us": round(res["separate"], 3)}
+    assert plan.error_flags() == 0
+    table["mlp_gate_up_swiglu:4-bit"] = {"K": K, "N": N, "group": group, "splits": plan.info()["splits"],
+                                         "copies": copies, "per_M": fused_row}
     print(json.dumps({"cost_table": table, "unit": "us/call", "launch": "cuda_graph", "out": "bf16"}))
 
 

@@ -39,7 +39,7 @@ MAX_SPLITS = 16
 EXPORTS = (
     "qmm_validate_desc", "qmm_workspace_bytes", "qmm_plan", "qmm_plan_get_info",
     "qmm_check_forward_args", "qmm_forward", "qmm_forward_banked", "qmm_unpack_codes",
-    "qmm_plan_error", "qmm_destroy", "qmm_status_string", "qmm_forward_noalloc",
+    "qmm_plan_error", "qmm_destroy", "qmm_status_string", "qmm_forward_noalloc", "qmm_forward_swiglu",
 )
 
 
@@ -76,6 +76,7 @@ def _load() -> ctypes.CDLL:
     lib.qmm_check_forward_args.argtypes = [ctypes.POINTER(QmmDesc), vp, i32, i32, pp, pp, pp, i64, i64, i32, i32, pp]
     lib.qmm_forward.argtypes = [vp, vp, i32, vp, vp, vp, i64, i64, i32, i32, vp, vp]
     lib.qmm_forward_banked.argtypes = [vp, vp, i32, i32, pp, pp, pp, i64, i64, i32, i32, pp, vp]
+    lib.qmm_forward_swiglu.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, vp, vp]
     lib.qmm_unpack_codes.argtypes = [vp, i64, i64, i32, vp, vp]
     lib.qmm_forward_noalloc.argtypes = [vp, i32, vp, vp, vp, i64, i64, i32, i32, i32, vp, vp]
     lib.qmm_plan_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -240,6 +241,18 @@ def forward_banked(plan: Plan, x, ws, ss, bs, outs, stream=None) -> None:
                                 ctypes.c_void_p(_stream_handle(stream)))
     if st != QMM_OK:
         raise QmmError(st, "qmm_forward_banked")
+
+
+def forward_swiglu(plan: Plan, x, w_gate, s_gate, b_gate, w_up, s_up, b_up, out, stream=None) -> None:
+    """out[M, N] = silu(qmm(x, gate weights)) * qmm(x, up weights) in one main-kernel
+    launch (qmm_forward_swiglu; the plan needs max_banks >= 2)."""
+    M = int(x.shape[0]) if x.dim() == 2 else 1
+    vp = ctypes.c_void_p
+    st = _lib().qmm_forward_swiglu(plan.handle, vp(_ptr(x)), M, vp(_ptr(w_gate)), vp(_ptr(s_gate)),
+                                   vp(_ptr(b_gate)), vp(_ptr(w_up)), vp(_ptr(s_up)), vp(_ptr(b_up)), plan.K,
+                                   plan.N, plan.bits, plan.group, vp(_ptr(out)), vp(_stream_handle(stream)))
+    if st != QMM_OK:
+        raise QmmError(st, "qmm_forward_swiglu")
 
 
 def check_forward_args(desc: QmmDesc, x_ptr: int, M: int, w_ptrs, s_ptrs, b_ptrs, K, N, bits, group,

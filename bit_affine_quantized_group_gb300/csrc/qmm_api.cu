@@ -99,7 +99,9 @@ size_t xprep_region_bytes(const qmm_desc* d) {
 }
 
 size_t partial_region_bytes(const qmm_desc* d, int splits) {
-    if (splits <= 1) return 0;
+    // unsliced plans with two or more banks keep room for the fused gate/up
+    // projection's fp32 gate results ([max_M][N])
+    if (splits <= 1) return d->max_banks >= 2 ? static_cast<size_t>(d->max_M) * d->N * sizeof(float) : 0;
     return static_cast<size_t>(d->max_banks) * splits * d->max_M * static_cast<size_t>(d->N) * sizeof(float);
 }
 
@@ -339,10 +341,13 @@ int qmm_check_forward_args(const qmm_desc* d, const void* x_bf16, int M, int n_b
     return QMM_OK;
 }
 
-int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks,
-                       const uint32_t* const* packed_w, const uint16_t* const* scales_f16,
-                       const uint16_t* const* biases_f16, int64_t K, int64_t N, int bits, int group,
-                       void* const* out, void* stream) {
+namespace {
+
+// Shared body of the banked and the fused gate/up entry points. With swiglu,
+// n_banks is 2 (gate, up) and out[1] is the one output.
+int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, const uint32_t* const* packed_w,
+                 const uint16_t* const* scales_f16, const uint16_t* const* biases_f16, int64_t K, int64_t N,
+                 int bits, int group, void* const* out, void* stream, bool swiglu) {
     if (p == nullptr) return QMM_ERR_INVALID_ARG;
     const int chk = qmm_check_forward_args(&p->d, x_bf16, M, n_banks, packed_w, scales_f16, biases_f16, K, N,
                                            bits, group, out);
@@ -372,8 +377,10 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
     h.sb_vec16 = h.sb_tma;
     h.unpack_magic = kF16x2_1024;
     h.banks = n_banks;
+    h.swiglu = swiglu ? 1 : 0;
+    h.gate = swiglu ? p->partial : nullptr;
     h.xprep_bytes = static_cast<int64_t>(p->C) * xprep_chunk_bytes(bits, group, mi == 0 ? 8 : 16);
-    h.rows_total = static_cast<int64_t>(n_banks) * p->splits * N;
+    h.rows_total = static_cast<int64_t>(swiglu ? 1 : n_banks) * p->splits * N;
 
     int64_t ctas = (h.rows_total + kSlab - 1) / kSlab;
     if (ctas > p->num_sms) ctas = p->num_sms;
@@ -422,11 +429,36 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
         rp.M = M;
         rp.splits = p->splits;
         rp.banks = n_banks;
+        rp.swiglu = swiglu ? 1 : 0;
         rp.out_bf16 = p->d.out_dtype == QMM_OUT_BF16 ? 1 : 0;
         for (int i = 0; i < n_banks; ++i) rp.out[i] = out[i];
-        if (launch_reduce(rp, static_cast<int64_t>(n_banks) * M * N, st) != cudaSuccess) return QMM_ERR_CUDA;
+        if (swiglu) rp.out[0] = out[1];
+        if (launch_reduce(rp, static_cast<int64_t>(swiglu ? 1 : n_banks) * M * N, st) != cudaSuccess)
+            return QMM_ERR_CUDA;
     }
     return QMM_OK;
+}
+
+}  // namespace
+
+int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks,
+                       const uint32_t* const* packed_w, const uint16_t* const* scales_f16,
+                       const uint16_t* const* biases_f16, int64_t K, int64_t N, int bits, int group,
+                       void* const* out, void* stream) {
+    return forward_impl(p, x_bf16, M, n_banks, packed_w, scales_f16, biases_f16, K, N, bits, group, out, stream,
+                        false);
+}
+
+int qmm_forward_swiglu(const qmm_plan_t* p, const void* x_bf16, int M, const uint32_t* w_gate,
+                       const uint16_t* s_gate, const uint16_t* b_gate, const uint32_t* w_up, const uint16_t* s_up,
+                       const uint16_t* b_up, int64_t K, int64_t N, int bits, int group, void* out, void* stream) {
+    if (p == nullptr) return QMM_ERR_INVALID_ARG;
+    if (p->d.max_banks < 2) return QMM_ERR_INVALID_ARG;   // the gate results live in the bank workspace
+    const uint32_t* w[2] = {w_gate, w_up};
+    const uint16_t* sc[2] = {s_gate, s_up};
+    const uint16_t* bi[2] = {b_gate, b_up};
+    void* o[2] = {out, out};
+    return forward_impl(p, x_bf16, M, 2, w, sc, bi, K, N, bits, group, o, stream, true);
 }
 
 int qmm_forward(const qmm_plan_t* p, const void* x_bf16, int M, const uint32_t* packed_w,

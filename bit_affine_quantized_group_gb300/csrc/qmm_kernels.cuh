@@ -74,6 +74,8 @@ struct MainHeader {
     int sb_tma;             // scales/biases by TMA boxes (G % 8 == 0), else cp.async
     int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
     int banks;
+    int swiglu;             // fused gate/up: banks 0 (gate) and 1 (up) of every row block, out = silu(gate) * up
+    float* gate;            // [M][N] fp32 gate results of the current call (swiglu, unsliced)
     uint32_t unpack_magic;  // kBf16x2_128, given at run time so it stays in a register
 };
 
@@ -93,6 +95,7 @@ struct ReduceParams {
     int splits;
     int banks;
     int out_bf16;
+    int swiglu;             // out[0] = silu(sum of bank 0) * (sum of bank 1)
     void* out[kMaxBanks];
 };
 
@@ -105,20 +108,24 @@ template <typename F>
 __device__ __forceinline__ void for_each_row_block(const MainHeader& p, F&& f) {
     const int64_t r_begin = p.rows_total * blockIdx.x / gridDim.x;
     const int64_t r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
+    // fused gate/up: the flattened space is (split, row) and every row block is
+    // run for bank 0 (gate) and then bank 1 (up) by the same CTA
+    const int passes = p.swiglu ? 2 : 1;
     int64_t r = r_begin;
     while (r < r_end) {
         const int64_t seg = r / p.N;                                  // bank * splits + split
         const int64_t seg_end = min(r_end, (seg + 1) * p.N);
         const int64_t len = seg_end - r;
         const int nb = static_cast<int>((len + kTN - 1) / kTN);
-        const int bank = static_cast<int>(seg / p.splits);
+        const int bank = p.swiglu ? 0 : static_cast<int>(seg / p.splits);
         const int split = static_cast<int>(seg % p.splits);
         const int c0 = static_cast<int>(static_cast<int64_t>(split) * p.C / p.splits);
         const int c1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.C / p.splits);
         for (int ib = 0; ib < nb; ++ib) {
             const int64_t a = r + len * ib / nb;
             const int64_t e = r + len * (ib + 1) / nb;
-            if (!f(bank, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
+            for (int pass = 0; pass < passes; ++pass)
+                if (!f(bank + pass, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
         }
         r = seg_end;
     }
@@ -689,13 +696,25 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                         for (int e = 0; e < 2; ++e) {
                             const int m = 8 * j + 2 * t + e;
                             if (m >= p.M) continue;
-                            const float v = acc[sw][j][2 * h + e] + sc[((sw * NT + j) * 4 + 2 * h + e) * 32 + lane];
+                            float v = acc[sw][j][2 * h + e] + sc[((sw * NT + j) * 4 + 2 * h + e) * 32 + lane];
+                            if (p.out_mode == kOutPartial) {
+                                p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
+                                continue;
+                            }
+                            if (p.swiglu) {
+                                // gate pass: keep the fp32 gate; up pass: the same thread
+                                // wrote this (m, n) gate in the gate pass of this row block
+                                if (bank == 0) {
+                                    p.gate[m * p.N + n] = v;
+                                    continue;
+                                }
+                                const float gv = p.gate[m * p.N + n];
+                                v = gv / (1.0f + expf(-gv)) * v;
+                            }
                             if (p.out_mode == kOutF32) {
                                 static_cast<float*>(bp.out)[m * p.N + n] = v;
-                            } else if (p.out_mode == kOutBF16) {
-                                static_cast<__nv_bfloat16*>(bp.out)[m * p.N + n] = __float2bfloat16_rn(v);
                             } else {
-                                p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
+                                static_cast<__nv_bfloat16*>(bp.out)[m * p.N + n] = __float2bfloat16_rn(v);
                             }
                         }
                     }

@@ -1,6 +1,7 @@
 // Split-K reduce kernel: out[bank][m][n] = sum over slices s = 0..S-1, in that
 // order, of the fp32 partials (vmlx-swift PR #565, "JANGH split-K verify tile"
-// commit: K slices write FP32 partials which are then summed).
+// commit: K slices write FP32 partials which are then summed). For the fused
+// gate/up projection it writes silu(gate sum) * (up sum) to the one output.
 #include "qmm_kernels.cuh"
 
 namespace qmmk {
@@ -8,7 +9,7 @@ namespace qmmk {
 __global__ void __launch_bounds__(kReduceThreads) qmm_splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     griddep_wait();   // partials of the main kernel are complete and visible
     const int64_t per_bank = static_cast<int64_t>(p.M) * p.N;
-    const int64_t total = per_bank * p.banks;
+    const int64_t total = per_bank * (p.swiglu ? 1 : p.banks);
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t bank = i / per_bank;
@@ -16,6 +17,13 @@ __global__ void __launch_bounds__(kReduceThreads) qmm_splitk_reduce_kernel(const
         const float* src = p.partial + bank * p.splits * per_bank + e;
         float s = src[0];
         for (int sp = 1; sp < p.splits; ++sp) s += src[sp * per_bank];
+        if (p.swiglu) {
+            // fused gate/up: bank 0 holds the gate slices, bank 1 the up slices
+            const float* usrc = p.partial + p.splits * per_bank + e;
+            float u = usrc[0];
+            for (int sp = 1; sp < p.splits; ++sp) u += usrc[sp * per_bank];
+            s = s / (1.0f + expf(-s)) * u;
+        }
         if (p.out_bf16)
             static_cast<__nv_bfloat16*>(p.out[bank])[e] = __float2bfloat16_rn(s);
         else

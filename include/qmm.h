@@ -47,7 +47,7 @@
  *
  * Conventions:
  *   - Every function returns a qmm_status (0 = QMM_OK) and never throws.
- *   - qmm_forward / qmm_forward_banked are asynchronous on `stream` (a
+ *   - qmm_forward / qmm_forward_banked / qmm_forward_swiglu are asynchronous on `stream` (a
  *     cudaStream_t passed as void*, NULL = legacy default stream); they never
  *     allocate and never synchronize. Errors in arguments are reported before
  *     anything is launched. Launch failures return QMM_ERR_CUDA.
@@ -174,6 +174,26 @@ int qmm_forward_banked(const qmm_plan_t* p, const void* x_bf16, int M, int n_ban
                        const uint32_t* const* packed_w, const uint16_t* const* scales_f16,
                        const uint16_t* const* biases_f16, int64_t K, int64_t N, int bits,
                        int group, void* const* out, void* stream);
+
+/*
+ * Fused gate/up projection with a SwiGLU epilogue ("Qwen3.8 Flash Next
+ * performance and parity receipt": the exact fused projection promoted over
+ * separate gate and up projections):
+ *   out[m, n] = silu(gate[m, n]) * up[m, n],   silu(g) = g / (1 + exp(-g)),
+ * where gate and up are the qmm_forward results of (w_gate, s_gate, b_gate)
+ * and (w_up, s_up, b_up) on the same x, both N x K in the plan's format. One
+ * launch of the main kernel computes both: every CTA runs each of its row
+ * blocks for the gate and then for the up weights, keeping the fp32 gate
+ * values in the plan's workspace. The plan must have max_banks >= 2 (else
+ * QMM_ERR_INVALID_ARG). With splits > 1 both projections write fp32 slice
+ * partials and the reduce kernel applies the epilogue to the slice sums.
+ * Pointers and argument checks as for qmm_forward; out is [M, N] in the
+ * plan's output type.
+ */
+int qmm_forward_swiglu(const qmm_plan_t* p, const void* x_bf16, int M, const uint32_t* w_gate,
+                       const uint16_t* s_gate, const uint16_t* b_gate, const uint32_t* w_up,
+                       const uint16_t* s_up, const uint16_t* b_up, int64_t K, int64_t N, int bits,
+                       int group, void* out, void* stream);
 
 /*
  * Diagnostic: run the main kernel's in-register code unpacking on packed

@@ -13,7 +13,7 @@
 // JANGH loading", LaneQMM commit: "C += s*P + b*XS"); that form is provided
 // separately (oracle_qmm_spbxs_f64) so the tests can check the identity.
 //
-// Storage conventions the pages leave open (readings stated in the design doc):
+// Storage conventions the pages leave open (the plainest readings, shared by the workloads):
 //   * codes q[n,k] are an LSB-first bit stream per row: bit j of code k is
 //     bit (k*bits+j) mod 32 of word (k*bits+j) / 32 of that row; a row spans
 //     K*bits/32 uint32 words and starts on a word boundary.
@@ -258,6 +258,29 @@ int oracle_qmm_spbxs_f64(const uint16_t* x_bf16, int64_t M, const uint32_t* word
                 y[m * N + n] = acc;
             }
         }
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Fused gate/up projection with a SwiGLU epilogue ("Qwen3.8 Flash Next
+// performance and parity receipt": the exact fused projection promoted over
+// separate gate and up projections):
+//   y[m,n] = silu(g[m,n]) * u[m,n],   silu(v) = v / (1 + exp(-v)),
+// g and u being the plain-definition results above for the gate weights and
+// the up weights on the same x.
+// ---------------------------------------------------------------------------
+int oracle_qmm_swiglu_f64(const uint16_t* x_bf16, int64_t M, const uint32_t* words_gate,
+                          const uint16_t* scales_gate, const uint16_t* biases_gate, const uint32_t* words_up,
+                          const uint16_t* scales_up, const uint16_t* biases_up, int64_t K, int64_t N, int bits,
+                          int group, double* y) {
+    if (check_qmm(M, K, N, bits, group)) return 1;
+    std::vector<double> g((size_t)(M * N)), u((size_t)(M * N));
+    if (oracle_qmm_f64(x_bf16, M, words_gate, scales_gate, biases_gate, K, N, bits, group, g.data())) return 1;
+    if (oracle_qmm_f64(x_bf16, M, words_up, scales_up, biases_up, K, N, bits, group, u.data())) return 1;
+    for (int64_t i = 0; i < M * N; ++i) {
+        const double v = g[(size_t)i];
+        y[i] = v / (1.0 + std::exp(-v)) * u[(size_t)i];
     }
     return 0;
 }

@@ -310,3 +310,88 @@ def test_oracle_rejects_bad_shapes():
     with pytest.raises(ValueError):
         o.qmm_f64(np.zeros((1, 48), np.uint16), np.zeros((1, 6), np.uint32),
                   np.zeros((1, 1), np.uint16), np.zeros((1, 1), np.uint16), 48, 1, 4, 32)
+
+
+# ---------------------------------------------------------------------------
+# Fused gate/up projection with the SwiGLU epilogue
+# ---------------------------------------------------------------------------
+def _silu_tanh(v: float) -> float:
+    """silu through a different closed form: v * sigmoid(v) = v * (1 + tanh(v/2)) / 2."""
+    import math
+    return v * (1.0 + math.tanh(v / 2.0)) / 2.0
+
+
+def test_swiglu_one_hot_matches_closed_form():
+    """One-hot x rows pick single dequantized weights, so g and u are exact
+    dyadic numbers; y must equal silu(g) * u evaluated through tanh."""
+    import math
+    o = _oracle()
+    bits, group, K, N = 4, 32, 64, 3
+    rng = np.random.default_rng(3)
+    cg = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    cu = rng.integers(0, 16, size=(N, K)).astype(np.uint8)
+    G = K // group
+    sg = np.full((N, G), 0.5, np.float16).view(np.uint16)
+    bg = np.full((N, G), -4.0, np.float16).view(np.uint16)
+    su = np.full((N, G), 0.25, np.float16).view(np.uint16)
+    bu = np.full((N, G), 1.0, np.float16).view(np.uint16)
+    ks = [0, 5, 33, 63]
+    x = np.zeros((len(ks), K), np.uint16)
+    for i, k in enumerate(ks):
+        x[i, k] = 0x3F80            # bfloat16 1.0
+    y = o.qmm_swiglu_f64(x, pack_rows(cg, bits), sg, bg, pack_rows(cu, bits), su, bu, K, N, bits, group)
+    for i, k in enumerate(ks):
+        for n in range(N):
+            g = 0.5 * float(cg[n, k]) - 4.0
+            u = 0.25 * float(cu[n, k]) + 1.0
+            want = _silu_tanh(g) * u
+            assert math.isclose(y[i, n], want, rel_tol=1e-14, abs_tol=1e-15), (i, n, y[i, n], want)
+            if g == 0.0:
+                assert y[i, n] == 0.0
+
+
+def test_swiglu_saturation():
+    """Large positive gates pass through (silu(g) = g in float64 for g >= 40);
+    large negative gates vanish."""
+    o = _oracle()
+    bits, group, K, N = 8, 32, 32, 2
+    codes = np.full((N, K), 0, np.uint8)
+    G = 1
+    sg = np.full((N, G), 1.0, np.float16).view(np.uint16)
+    bg = np.array([[40.0], [-40.0]], np.float16).view(np.uint16)
+    su = np.full((N, G), 1.0, np.float16).view(np.uint16)
+    bu = np.full((N, G), 3.0, np.float16).view(np.uint16)
+    x = np.zeros((1, K), np.uint16)
+    x[0, 7] = 0x3F80
+    y = o.qmm_swiglu_f64(x, pack_rows(codes, bits), sg, bg, pack_rows(codes, bits), su, bu, K, N, bits, group)
+    assert y[0, 0] == 120.0
+    assert 0.0 > y[0, 1] > -1e-14
+
+
+def test_swiglu_brute_force_tiny():
+    """Random tiny case against a triple loop written here (dequantize, dot,
+    silu through exp)."""
+    import math
+    import datagen
+    o = _oracle()
+    bits, group, K, N, M = 5, 32, 64, 3, 2
+    a = datagen.gen_qmm(41, M, K, N, bits, group)
+    c = datagen.gen_qmm(42, M, K, N, bits, group)
+    y = o.qmm_swiglu_f64(a.x, a.words[0], a.scales[0], a.biases[0], c.words[0], c.scales[0], c.biases[0],
+                         K, N, bits, group)
+    xs = (a.x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    def proj(inp):
+        codes = o.decode_bitwise(inp.words[0], N, K, bits).astype(np.float64)
+        s = inp.scales[0].view(np.float16).astype(np.float64)
+        b = inp.biases[0].view(np.float16).astype(np.float64)
+        out = np.zeros((M, N))
+        for m in range(M):
+            for n in range(N):
+                out[m, n] = sum(xs[m, k] * (s[n, k // group] * codes[n, k] + b[n, k // group]) for k in range(K))
+        return out
+    g, u = proj(a), proj(c)
+    for m in range(M):
+        for n in range(N):
+            want = g[m, n] / (1.0 + math.exp(-g[m, n])) * u[m, n]
+            assert math.isclose(y[m, n], want, rel_tol=1e-11, abs_tol=1e-12)
