@@ -120,14 +120,14 @@ cudaError_t configure(int bits, int group, int mb, int smem) {
 }
 
 cudaError_t launch(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,
-                   const MainParams<kMaxBanks>* banked) {
+                   const MainParams<kMaxBanks>* banked, const MainParams<2>* fused = nullptr) {
     switch (bits) {
-        case 2: return launch_forward<2>(group, L, single, banked);
-        case 3: return launch_forward<3>(group, L, single, banked);
-        case 4: return launch_forward<4>(group, L, single, banked);
-        case 5: return launch_forward<5>(group, L, single, banked);
-        case 6: return launch_forward<6>(group, L, single, banked);
-        case 8: return launch_forward<8>(group, L, single, banked);
+        case 2: return launch_forward<2>(group, L, single, banked, fused);
+        case 3: return launch_forward<3>(group, L, single, banked, fused);
+        case 4: return launch_forward<4>(group, L, single, banked, fused);
+        case 5: return launch_forward<5>(group, L, single, banked, fused);
+        case 6: return launch_forward<6>(group, L, single, banked, fused);
+        case 8: return launch_forward<8>(group, L, single, banked, fused);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -408,7 +408,12 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
         return true;
     };
     cudaError_t le;
-    if (n_banks == 1) {
+    if (swiglu) {
+        MainParams<2> mp2;
+        std::memset(&mp2, 0, sizeof(mp2));
+        if (!fill(mp2)) return QMM_ERR_CUDA;
+        le = launch(bits, group, L, nullptr, nullptr, &mp2);
+    } else if (n_banks == 1) {
         MainParams<1> mp1;
         std::memset(&mp1, 0, sizeof(mp1));
         if (!fill(mp1)) return QMM_ERR_CUDA;

@@ -12,6 +12,9 @@ cudaError_t configure_one(int smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, kMaxBanks>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
@@ -43,8 +46,11 @@ cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
 }
 
 template <int BITS, int GROUP, int MB>
-cudaError_t launch_cap(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked) {
-    return single ? launch_one<BITS, GROUP, MB, 1>(L, *single) : launch_one<BITS, GROUP, MB, kMaxBanks>(L, *banked);
+cudaError_t launch_cap(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked,
+                       const MainParams<2>* fused) {
+    if (single) return launch_one<BITS, GROUP, MB, 1>(L, *single);
+    if (fused) return launch_one<BITS, GROUP, MB, 2>(L, *fused);
+    return launch_one<BITS, GROUP, MB, kMaxBanks>(L, *banked);
 }
 }  // namespace
 
@@ -58,12 +64,14 @@ cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, int smem_bytes) 
 
 template <>
 cudaError_t launch_forward<QMM_INST_BITS>(int group, const LaunchCfg& L, const MainParams<1>* single,
-                                          const MainParams<kMaxBanks>* banked) {
+                                          const MainParams<kMaxBanks>* banked, const MainParams<2>* fused) {
     constexpr int B = QMM_INST_BITS;
     if (group == 32)
-        return L.mb == 8 ? launch_cap<B, 32, 8>(L, single, banked) : launch_cap<B, 32, 16>(L, single, banked);
+        return L.mb == 8 ? launch_cap<B, 32, 8>(L, single, banked, fused)
+                         : launch_cap<B, 32, 16>(L, single, banked, fused);
     if (group == 64)
-        return L.mb == 8 ? launch_cap<B, 64, 8>(L, single, banked) : launch_cap<B, 64, 16>(L, single, banked);
+        return L.mb == 8 ? launch_cap<B, 64, 8>(L, single, banked, fused)
+                         : launch_cap<B, 64, 16>(L, single, banked, fused);
     return cudaErrorInvalidValue;
 }
 

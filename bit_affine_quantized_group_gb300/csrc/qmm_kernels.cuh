@@ -74,7 +74,7 @@ struct MainHeader {
     int sb_tma;             // scales/biases by TMA boxes (G % 8 == 0), else cp.async
     int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
     int banks;
-    int swiglu;             // fused gate/up: banks 0 (gate) and 1 (up) of every row block, out = silu(gate) * up
+    int swiglu;             // fused gate/up (the two-bank kernel): out = silu(gate) * up
     float* gate;            // [M][N] fp32 gate results of the current call (swiglu, unsliced)
     uint32_t unpack_magic;  // kBf16x2_128, given at run time so it stays in a register
 };
@@ -104,28 +104,31 @@ struct ReduceParams {
 // (bank, split, row) space is cut evenly over the CTAs; a CTA's range is cut at
 // (bank, split) boundaries and then into balanced row blocks of <= kTN rows.
 // ---------------------------------------------------------------------------
-template <typename F>
+template <bool SWIGLU, typename F>
 __device__ __forceinline__ void for_each_row_block(const MainHeader& p, F&& f) {
     const int64_t r_begin = p.rows_total * blockIdx.x / gridDim.x;
     const int64_t r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
-    // fused gate/up: the flattened space is (split, row) and every row block is
-    // run for bank 0 (gate) and then bank 1 (up) by the same CTA
-    const int passes = p.swiglu ? 2 : 1;
     int64_t r = r_begin;
     while (r < r_end) {
         const int64_t seg = r / p.N;                                  // bank * splits + split
         const int64_t seg_end = min(r_end, (seg + 1) * p.N);
         const int64_t len = seg_end - r;
         const int nb = static_cast<int>((len + kTN - 1) / kTN);
-        const int bank = p.swiglu ? 0 : static_cast<int>(seg / p.splits);
+        // fused gate/up: the flattened space is (split, row) and every row block
+        // is run for bank 0 (gate) and then bank 1 (up) by the same CTA
+        const int bank = SWIGLU ? 0 : static_cast<int>(seg / p.splits);
         const int split = static_cast<int>(seg % p.splits);
         const int c0 = static_cast<int>(static_cast<int64_t>(split) * p.C / p.splits);
         const int c1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.C / p.splits);
         for (int ib = 0; ib < nb; ++ib) {
             const int64_t a = r + len * ib / nb;
             const int64_t e = r + len * (ib + 1) / nb;
-            for (int pass = 0; pass < passes; ++pass)
-                if (!f(bank + pass, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
+            if constexpr (SWIGLU) {
+                if (!f(0, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
+                if (!f(1, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
+            } else {
+                if (!f(bank, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
+            }
         }
         r = seg_end;
     }
@@ -321,6 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     constexpr int SB = stage_bytes(BITS, GROUP, MB);
     constexpr int NV = kGroupsPerWarp * VB;        // k32 blocks per consumer warp per stage
     const MainHeader& p = P.h;
+    // the two-bank parameter block is the fused gate/up projection's
+    constexpr bool SWIGLU = CAP == 2;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                 for (int i = 0; i < npend; ++i) issue_xprep(pend_slot[i], pend_chunk[i]);
             npend = 0;
         };
-        for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
+        for_each_row_block<SWIGLU>(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
             (void)split;
             const BankPtrs bp = P.bank[bank];
             // the cp.async path for scales/biases checks its buffers once per row block
@@ -481,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     int cslot = 0;            // stage index % S, kept incrementally
     uint32_t cphase = 0;      // (stage index / S) & 1
     bool ok = true;
-    for_each_row_block(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
+    for_each_row_block<SWIGLU>(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
         const int nsl = (rows + kSlab - 1) / kSlab;
         bool act[kSPW];
         int row0[kSPW];
@@ -701,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                                 p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
                                 continue;
                             }
-                            if (p.swiglu) {
+                            if constexpr (SWIGLU) {
                                 // gate pass: keep the fp32 gate; up pass: the same thread
                                 // wrote this (m, n) gate in the gate pass of this row block
                                 if (bank == 0) {
@@ -786,7 +791,8 @@ cudaError_t configure_kernels(int group, int mb, int smem_bytes);
 // Weight-box width for a format (host side, for encoding tensor maps).
 inline int weight_box_width(int bits, int group) { return wbox_width(bits, group); }
 template <int BITS>
-cudaError_t launch_forward(int group, const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked);
+cudaError_t launch_forward(int group, const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked,
+                           const MainParams<2>* fused);
 template <int BITS>
 cudaError_t launch_unpack(const uint32_t* w, int64_t K, int64_t N, uint8_t* codes, cudaStream_t stream);
 

@@ -66,12 +66,12 @@ cudaError_t configure_format(int bits, int group, int mb, int smem) {
 
 cudaError_t launch_format(int bits, int group, const LaunchCfg& L, const MainParams<1>* mp) {
     switch (bits) {
-        case 2: return launch_forward<2>(group, L, mp, nullptr);
-        case 3: return launch_forward<3>(group, L, mp, nullptr);
-        case 4: return launch_forward<4>(group, L, mp, nullptr);
-        case 5: return launch_forward<5>(group, L, mp, nullptr);
-        case 6: return launch_forward<6>(group, L, mp, nullptr);
-        default: return launch_forward<8>(group, L, mp, nullptr);
+        case 2: return launch_forward<2>(group, L, mp, nullptr, nullptr);
+        case 3: return launch_forward<3>(group, L, mp, nullptr, nullptr);
+        case 4: return launch_forward<4>(group, L, mp, nullptr, nullptr);
+        case 5: return launch_forward<5>(group, L, mp, nullptr, nullptr);
+        case 6: return launch_forward<6>(group, L, mp, nullptr, nullptr);
+        default: return launch_forward<8>(group, L, mp, nullptr, nullptr);
     }
 }
 
