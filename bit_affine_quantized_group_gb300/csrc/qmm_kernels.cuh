@@ -8,10 +8,11 @@
 //                            commit) as split binary16 fragments, and one
 //                            power-of-two range factor per (row, chunk).
 //   2. qmm_main_kernel    -- one CTA per SM; a producer warp streams packed code
-//                            rows, scales and biases (16-byte cp.async pieces)
-//                            and the staged activations (one TMA bulk copy per
-//                            chunk) into a ring of
-//                            shared-memory stages; four consumer warps unpack the
+//                            rows (TMA 2-D tensor boxes), scales and biases (TMA
+//                            boxes, or 4-byte cp.async pieces when a row of them
+//                            is not 16-byte aligned) and the staged activations
+//                            (one bulk copy per chunk) into a ring of shared-
+//                            memory stages; eight consumer warps unpack the
 //                            codes in registers and contract them on tensor cores,
 //                            reading each code byte once for all M rows (same
 //                            page, qwen_qmv_rows_full commit: weights read once per
@@ -76,7 +77,7 @@ struct MainHeader {
     int banks;
     int swiglu;             // fused gate/up (the two-bank kernel): out = silu(gate) * up
     float* gate;            // [M][N] fp32 gate results of the current call (swiglu, unsliced)
-    uint32_t unpack_magic;  // kBf16x2_128, given at run time so it stays in a register
+    uint32_t unpack_magic;  // kF16x2_1024, given at run time so it stays in a register
 };
 
 template <int CAP>
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
     const int sp = warp % kSlabPairs;        // slabs sp and sp + 4
     const int kh = warp / kSlabPairs;        // chunk groups 4*kh .. 4*kh + 3
     const int gbase = kh * kGroupsPerWarp;
-    const int vbw = gbase * VB;              // first virtual block of this warp in a chunk
+    const int vbw = gbase * VB;              // first k32 block of this warp in a chunk
     // Offsets of this lane's codes in each of the warp's k32 blocks, for a tile
     // row r with r % 8 == 0 (add r * W): box base + swizzled 16-byte chunk +
     // byte. 4-bit: one word (block = one 16-byte chunk); 8-bit: two words
