@@ -143,11 +143,32 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
 }
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t v) { return __uint_as_float(v << 16); }
 
+// 16 bytes of x through L2 (x may have been written on other SMs just before).
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// One CTA per chunk, one warp per scale group of the chunk. For 8-row tile j,
+// lane (g, t) of warp gg holds activation row m = 8j + g and, of each k32 block
+// vb of the group, the 8-code piece 4vb + t (codes 32vb + 8t .. 32vb + 8t + 7),
+// so the four lanes of a quad hold the group's codes of one row:
+//   XS[m,g]  = sum_{k in g} x[m,k],   XSc[m,g] = sum_{k in g} x[m,k] * 1024 * 2^-j(k),
+// summed over each piece in code order, then over the lane's pieces and the
+// quad in a fixed tree order. f = 2^(14 - e) from the binary exponent e of the
+// chunk's largest |x| (clamped so f and 1/f stay normal), sigma = 2^(e' - 13)
+// from the largest |XS|, |XSc| of the chunk (exponent e'), both over the eight
+// groups through shared memory. Rows m >= M and codes past the end of K stage
+// as zeros (f = sigma = 1).
 template <int BITS, int GROUP, int MB>
 __global__ void __launch_bounds__(kXprepThreads)
 qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_t* __restrict__ xprep) {
+    static_assert(kXprepThreads == 32 * kGPC, "one warp per scale group");
     constexpr int CK = kGPC * GROUP;                 // codes per chunk
-    constexpr int KB = vblocks_per_chunk(BITS, GROUP);
+    constexpr int VPG = GROUP / 32;                  // k32 blocks per group
     constexpr int NT = n8_tiles(MB);
     constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
     constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
@@ -159,135 +180,136 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     griddep_launch_dependents();
     griddep_wait();
 
-    __shared__ __align__(16) uint16_t xs[MB][CK];
-    __shared__ float xsum[MB][kGPC];     // XS
-    __shared__ float xsc[MB][kGPC];      // XSc
-    __shared__ uint32_t xmag[MB][kGPC];  // largest |x| bit pattern of the group
-    __shared__ float rsig[MB];           // 1 / sigma
-    __shared__ float fsc[MB];            // f
+    __shared__ float s_xs[MB][kGPC];      // XS
+    __shared__ float s_xsc[MB][kGPC];     // XSc
+    __shared__ uint32_t s_mag[MB][kGPC];  // largest |x| bit pattern of the group
 
     const int c = blockIdx.x;
-    const int g0 = c * kGPC;
-    const int ng = min(kGPC, G - g0);
-    const int64_t k0 = static_cast<int64_t>(g0) * GROUP;
-    const int kc = ng * GROUP;
-    const int tid = threadIdx.x;
+    const int gg = threadIdx.x >> 5;                 // this warp's group
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int64_t k0 = static_cast<int64_t>(c) * CK;
+    const int kc = min(kGPC, G - c * kGPC) * GROUP;  // codes of this chunk inside K
+    const bool x16 = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
 
-    if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
-        // rows are 2K bytes apart and chunks start 16-byte aligned: 16-byte loads,
-        // all issued before any is used
-        constexpr int V8 = CK / 8;                          // 16-byte pieces per row
-        constexpr int PER = (MB * V8 + kXprepThreads - 1) / kXprepThreads;
-        uint4 v[PER];
+    // every load first
+    uint4 v[NT][VPG];
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int i = tid + u * kXprepThreads;
-            const int m = i / V8, kk = (i - (i / V8) * V8) * 8;
-            v[u] = make_uint4(0, 0, 0, 0);
-            if (i < MB * V8 && m < M && kk < kc)
-                v[u] = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(m) * K + k0 + kk);
-        }
+    for (int j = 0; j < NT; ++j) {
+        const int m = 8 * j + g;
+        const uint16_t* row = x + static_cast<int64_t>(m) * K + k0;
 #pragma unroll
-        for (int u = 0; u < PER; ++u) {
-            const int i = tid + u * kXprepThreads;
-            if (i < MB * V8) reinterpret_cast<uint4*>(&xs[0][0])[i] = v[u];
-        }
-    } else {
-        for (int i = tid; i < MB * CK; i += blockDim.x) {
-            const int m = i / CK, k = i - (i / CK) * CK;
-            xs[m][k] = (m < M && k < kc) ? x[static_cast<int64_t>(m) * K + k0 + k] : static_cast<uint16_t>(0);
+        for (int u = 0; u < VPG; ++u) {
+            const int k = 32 * (gg * VPG + u) + 8 * t;
+            v[j][u] = make_uint4(0, 0, 0, 0);
+            if (m < M && k < kc) {
+                if (x16) {
+                    v[j][u] = ld_cg_v4(row + k);
+                } else {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        w[e] = static_cast<uint32_t>(__ldcg(row + k + 2 * e)) |
+                               (static_cast<uint32_t>(__ldcg(row + k + 2 * e + 1)) << 16);
+                    v[j][u] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
         }
     }
-    __syncthreads();
-    if (tid < MB * kGPC) {
-        // XS, XSc and the largest magnitude of one (row, group), 8 codes at a time
-        // (code k of a k32 block has mantissa shift j = code_shift(k % 8))
-        const int m = tid / kGPC, gg = tid % kGPC;
+    // group sums and magnitude of each row
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
         float s = 0.0f, sc = 0.0f;
         uint32_t mag = 0;
-        const uint4* src = reinterpret_cast<const uint4*>(&xs[m][gg * GROUP]);
 #pragma unroll
-        for (int u = 0; u < GROUP / 8; ++u) {
-            const uint4 q = src[u];
-            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        for (int u = 0; u < VPG; ++u) {
+            const uint32_t wv[4] = {v[j][u].x, v[j][u].y, v[j][u].z, v[j][u].w};
+            float ps = 0.0f, psc = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const uint32_t hbits = (wv[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
                 const float xv = bf16_bits_to_float(hbits);
-                s += xv;
-                sc = fmaf(xv, 1024.0f / static_cast<float>(1 << code_shift(BITS, e)), sc);
+                ps += xv;
+                psc = fmaf(xv, 1024.0f / static_cast<float>(1 << code_shift(BITS, e)), psc);
                 mag = max(mag, hbits & 0x7FFFu);
             }
+            s = u == 0 ? ps : s + ps;
+            sc = u == 0 ? psc : sc + psc;
         }
-        xsum[m][gg] = s;
-        xsc[m][gg] = sc;
-        xmag[m][gg] = mag;
-    }
-    __syncthreads();
-    if (tid < MB) {
-        float amax = 0.0f;
-        uint32_t mag = 0;
-        for (int gg = 0; gg < kGPC; ++gg) {
-            amax = fmaxf(amax, fmaxf(fabsf(xsum[tid][gg]), fabsf(xsc[tid][gg])));
-            mag = max(mag, xmag[tid][gg]);
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
+        sc += __shfl_xor_sync(0xFFFFFFFFu, sc, 1);
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
+        sc += __shfl_xor_sync(0xFFFFFFFFu, sc, 2);
+        mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));
+        mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 2));
+        if (t == 0) {
+            s_xs[8 * j + g][gg] = s;
+            s_xsc[8 * j + g][gg] = sc;
+            s_mag[8 * j + g][gg] = mag;
         }
-        // sigma = 2^(e-13) puts the largest |XS/sigma|, |XSc/sigma| in [2^13, 2^14):
-        // inside the binary16 range with room to spare.
-        float sg = 1.0f;
-        if (amax > 0.0f && amax <= 3.0e38f) sg = ldexpf(1.0f, ilogbf(amax) - 13);
-        rsig[tid] = 1.0f / sg;    // exact: power of two
-        // f = 2^(14 - e), e the binary exponent of the chunk's largest |x| (read
-        // off its bf16 bit pattern; clamped so f and 1/f stay normal floats):
-        // every f*x*2^-j is then below 2^15, and any x within 2^27 of the
-        // largest is exact in binary16.
-        int e = 0;
-        if (mag != 0) e = min(127, max(-100, static_cast<int>(mag >> 7) - 127));
-        const float f = (mag != 0) ? ldexpf(1.0f, 14 - e) : 1.0f;
-        fsc[tid] = f;
-        float* tail = reinterpret_cast<float*>(xprep + static_cast<size_t>(c) * XPB + XFB + xprep_bias_bytes(MB));
-        tail[tid] = sg;
-        tail[MB + tid] = 1.0f / f;  // exact: power of two
     }
     __syncthreads();
 
     uint8_t* out = xprep + static_cast<size_t>(c) * XPB;
     uint4* frag = reinterpret_cast<uint4*>(out);
-    for (int i = tid; i < KB * NT * 32; i += blockDim.x) {
-        // lane (g, t) of 8-row tile j, k32 block vb: activation row 8j + g,
-        // codes 32vb + 8t .. 32vb + 8t + 7 in the unpackers' slot order
-        const int lane = i & 31;
-        const int j = (i >> 5) % NT;
-        const int vb = (i >> 5) / NT;
-        const int t = lane & 3;
-        const int m = 8 * j + (lane >> 2);
-        const int kb = 32 * vb + 8 * t;
-        const float f = fsc[m];
-        uint32_t r[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float lo = bf16_bits_to_float(xs[m][kb + slot_code(BITS, q, 0)]) * f *
-                             (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 0)));
-            const float hi = bf16_bits_to_float(xs[m][kb + slot_code(BITS, q, 1)]) * f *
-                             (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 1)));
-            r[q] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
-        }
-        frag[i] = make_uint4(r[0], r[1], r[2], r[3]);
-    }
     uint4* bias = reinterpret_cast<uint4*>(out + XFB);
-    for (int i = tid; i < NT * 32; i += blockDim.x) {
-        const int lane = i & 31;
-        const int j = i >> 5;
-        const int t = lane & 3;
-        const int m = 8 * j + (lane >> 2);
-        const float v0 = xsum[m][2 * t] * rsig[m];
-        const float v1 = xsum[m][2 * t + 1] * rsig[m];
-        const float w0 = -xsc[m][2 * t] * rsig[m];
-        const float w1 = -xsc[m][2 * t + 1] * rsig[m];
-        const __half v0h = __float2half_rn(v0), v1h = __float2half_rn(v1);
-        const __half w0h = __float2half_rn(w0), w1h = __float2half_rn(w1);
-        const __half v0l = __float2half_rn(v0 - __half2float(v0h)), v1l = __float2half_rn(v1 - __half2float(v1h));
-        const __half w0l = __float2half_rn(w0 - __half2float(w0h)), w1l = __float2half_rn(w1 - __half2float(w1h));
-        bias[i] = make_uint4(pack_half2(v0h, v1h), pack_half2(w0h, w1h), pack_half2(v0l, v1l), pack_half2(w0l, w1l));
+    float* tail = reinterpret_cast<float*>(out + XFB + xprep_bias_bytes(MB));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int m = 8 * j + g;
+        float amax = 0.0f;
+        uint32_t mag = 0;
+#pragma unroll
+        for (int q = 0; q < kGPC; ++q) {
+            amax = fmaxf(amax, fmaxf(fabsf(s_xs[m][q]), fabsf(s_xsc[m][q])));
+            mag = max(mag, s_mag[m][q]);
+        }
+        // sigma puts the largest |XS/sigma|, |XSc/sigma| in [2^13, 2^14): inside the
+        // binary16 range with room to spare
+        float sg = 1.0f;
+        if (amax > 0.0f && amax <= 3.0e38f) sg = ldexpf(1.0f, ilogbf(amax) - 13);
+        const float rsig = 1.0f / sg;    // exact: power of two
+        // every f*x*2^-j is below 2^15, and any x within 2^27 of the largest is
+        // exact in binary16
+        int ex = 0;
+        if (mag != 0) ex = min(127, max(-100, static_cast<int>(mag >> 7) - 127));
+        const float f = (mag != 0) ? ldexpf(1.0f, 14 - ex) : 1.0f;
+        if (gg == 0 && t == 0) {
+            tail[m] = sg;
+            tail[MB + m] = 1.0f / f;   // exact: power of two
+        }
+        // MMA B fragments of this group's k32 blocks, in the unpackers' slot order
+#pragma unroll
+        for (int u = 0; u < VPG; ++u) {
+            const int vb = gg * VPG + u;
+            const uint32_t wv[4] = {v[j][u].x, v[j][u].y, v[j][u].z, v[j][u].w};
+            uint32_t r[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c0 = slot_code(BITS, q, 0), c1 = slot_code(BITS, q, 1);
+                const float lo = bf16_bits_to_float((wv[c0 >> 1] >> (16 * (c0 & 1))) & 0xFFFFu) * f *
+                                 (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 0)));
+                const float hi = bf16_bits_to_float((wv[c1 >> 1] >> (16 * (c1 & 1))) & 0xFFFFu) * f *
+                                 (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 1)));
+                r[q] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
+            }
+            frag[(vb * NT + j) * 32 + lane] = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+        // bias-term fragments of tile j (warp j): groups 2t and 2t + 1 of row m,
+        // XS and -XSc over sigma, each as a high and a low binary16 half
+        if (gg == j) {
+            const float v0 = s_xs[m][2 * t] * rsig;
+            const float v1 = s_xs[m][2 * t + 1] * rsig;
+            const float w0 = -s_xsc[m][2 * t] * rsig;
+            const float w1 = -s_xsc[m][2 * t + 1] * rsig;
+            const __half v0h = __float2half_rn(v0), v1h = __float2half_rn(v1);
+            const __half w0h = __float2half_rn(w0), w1h = __float2half_rn(w1);
+            const __half v0l = __float2half_rn(v0 - __half2float(v0h)), v1l = __float2half_rn(v1 - __half2float(v1h));
+            const __half w0l = __float2half_rn(w0 - __half2float(w0h)), w1l = __float2half_rn(w1 - __half2float(w1h));
+            bias[j * 32 + lane] =
+                make_uint4(pack_half2(v0h, v1h), pack_half2(w0h, w1h), pack_half2(v0l, v1l), pack_half2(w0l, w1l));
+        }
     }
 }
 
