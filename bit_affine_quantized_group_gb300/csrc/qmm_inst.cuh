@@ -21,9 +21,15 @@ cudaError_t configure_one(int smem_bytes) {
 
 template <int BITS, int GROUP, int MB, int CAP>
 cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
-    // Both kernels are programmatic dependents of what precedes them on the
-    // stream: each may be scheduled while its predecessor still runs and waits
-    // (griddepcontrol.wait) before touching anything the predecessor produces.
+    // The main kernel is a programmatic dependent of the staging kernel: it is
+    // scheduled once every staging CTA has started and waits (griddepcontrol.wait)
+    // before touching what the staging kernel writes. For up to 8 rows the staging
+    // kernel is a programmatic dependent of what precedes it too, and so resident
+    // (waiting) before that work ends. For 9..16 rows it is an ordinary launch:
+    // launched early, its CTAs take the first SMs the previous main kernel frees,
+    // a few to an SM, and the next main kernel's CTAs on those SMs wait for them to
+    // exit; that costs more than the later start (22.9 against 24.4 us/call on a
+    // 5120 x 17408 projection, the same within 1% on the other shapes measured).
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -34,10 +40,11 @@ cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     cfg.dynamicSmemBytes = 0;
     cfg.stream = L.stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = MB == 16 ? 0 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_xprep_kernel<BITS, GROUP, MB>, L.x, L.M, mp.h.K, mp.h.G,
                                        const_cast<uint8_t*>(mp.h.xprep));
     if (e != cudaSuccess) return e;
+    cfg.numAttrs = 1;
     // (2) main kernel: loads weights at once, waits for (1) before its staged activations
     cfg.gridDim = dim3(static_cast<unsigned>(L.ctas));
     cfg.blockDim = dim3(kThreads);

@@ -173,9 +173,9 @@ qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_
     constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
     constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
 
-    // The main kernel may start loading weights while this runs. This kernel is
-    // itself launched as a programmatic dependent of whatever ran before it on the
-    // stream, so it must wait for that work (which may produce x, or still read
+    // The main kernel may start loading weights while this runs. This kernel may
+    // itself be launched as a programmatic dependent of whatever ran before it on
+    // the stream, so it waits for that work (which may produce x, or still read
     // the staging buffer) before touching x or the buffer.
     griddep_launch_dependents();
     griddep_wait();
