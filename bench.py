@@ -267,39 +267,60 @@ def run_gpu(args, ws, rank, local):
     # end to end through the public call with host buffers: each step copies its
     # input x (pinned host -> device, once per step: every call of the step reads
     # rows of the same x), runs the 40 calls, and reads every call's output back
-    # into pinned host memory after the last call, all on the calls' stream (an
-    # event or a copy between two calls would break the programmatic-dependent
-    # launch overlap of consecutive calls).
+    # into pinned host memory. The 40 outputs of a step are consecutive views of
+    # one device buffer, read back with one copy on a second stream once the step's
+    # last call is done, so the read-back overlaps the next step's calls (two
+    # output buffers alternate between steps; nothing is inserted between two
+    # calls of a step, which would break their programmatic-dependent launch
+    # overlap). The timed region ends when the last step's read-back has landed.
     x_pin = torch.from_numpy(x_host.view(np.int16)).pin_memory()
     x_dev = torch.empty((16, K), dtype=torch.int16, device=dev)
-    outs_e2e = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M, _ in calls]
-    y_pin = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for M, _ in calls]
+    total_rows = sum(M for M, _ in calls)
+    y_dev = [torch.empty((total_rows * N,), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    y_host = [torch.empty((total_rows * N,), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    outs_e2e = []
+    for buf in y_dev:
+        views, off = [], 0
+        for M, _ in calls:
+            views.append(buf[off:off + M * N].view(M, N))
+            off += M * N
+        outs_e2e.append(views)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    calls_done = [torch.cuda.Event() for _ in range(2)]
+    read_done = [torch.cuda.Event() for _ in range(2)]
     e2e_steps = max(5, min(args.steps, 200))
     h2d = 16 * K * 2
     d2h = sum(M * N * 2 for M, _ in calls)
 
-    def e2e_step():
+    def e2e_step(i):
+        b = i % 2
         with torch.cuda.stream(stream):
+            stream.wait_event(read_done[b])      # the buffer's previous read-back has landed
             x_dev.copy_(x_pin, non_blocking=True)
-            for i, (M, c) in enumerate(calls):
-                q.forward(plan, x_dev[:M].view(torch.bfloat16), W[c], S[c], B[c], outs_e2e[i], stream=stream)
-            for i in range(len(calls)):
-                y_pin[i].copy_(outs_e2e[i], non_blocking=True)
+            for j, (M, c) in enumerate(calls):
+                q.forward(plan, x_dev[:M].view(torch.bfloat16), W[c], S[c], B[c], outs_e2e[b][j], stream=stream)
+            calls_done[b].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(calls_done[b])
+            y_host[b].copy_(y_dev[b], non_blocking=True)
+            read_done[b].record(d2h_stream)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    for i in range(e2e_steps):
+        e2e_step(i)
     stream.synchronize()
+    d2h_stream.synchronize()
     e2e_sec = time.perf_counter() - t0
     e2e_units, e2e_max = aggregate(dist, step_bytes * e2e_steps / 1e9, e2e_sec)
     e2e_value = e2e_units / e2e_max
-    # the outputs read back are the call results (check one against the device copy)
-    if not torch.equal(y_pin[-1], outs_e2e[-1].cpu()):
+    # the outputs read back are the call results (check against the device copy)
+    last = (e2e_steps - 1) % 2
+    if not torch.equal(y_host[last], y_dev[last].cpu()):
         raise RuntimeError("end-to-end read-back differs from the device result")
 
     flags = plan.error_flags()
@@ -338,7 +359,7 @@ def run_gpu(args, ws, rank, local):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "launch": "direct",
-                "copies": "x host->device once per step; every call's y device->host after the step's calls"},
+                "copies": "x host->device once per step; every call's y device->host in one copy per step, overlapping the next step's calls"},
         "gpu_launches": kernels_per_call * len(calls) * args.steps,
         "clocks": clk,
     }
