@@ -157,6 +157,14 @@ int qmm_check_forward_args(const qmm_desc* d, const void* x_bf16, int M, int n_b
  * (QMM_ERR_PLAN_MISMATCH otherwise); M must be <= the plan's max_M.
  * Launches, in stream order: an activation-staging kernel, the main kernel
  * and, when the plan's splits > 1, the split-K reduce kernel.
+ *
+ * Ordering: x is read only after the work issued before the call on the
+ * stream has finished, and out is written after that too. The packed weights,
+ * scales and biases are streamed from the start (programmatic dependent
+ * launch), possibly while that earlier work still runs: they must not be
+ * written by work issued just before the call (weights are normally written
+ * once, at load time; synchronize the stream or record/wait an event in
+ * between otherwise). The same holds for every forward entry point.
  */
 int qmm_forward(const qmm_plan_t* p, const void* x_bf16, int M, const uint32_t* packed_w,
                 const uint16_t* scales_f16, const uint16_t* biases_f16, int64_t K, int64_t N,
