@@ -98,14 +98,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
-// Same with an L2 evict-first hint (for data read exactly once).
-__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                                uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
 // 2-D TMA tile load: the box at element coordinates (x, y) of `map` into shared
 // memory at dst (aligned to the map's swizzle atom), completion counted in bytes
 // on `bar`. x times the element size must be a multiple of 16 bytes.
@@ -125,15 +117,8 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-// Per-thread asynchronous copies (LDGSTS).
-// 16 bytes, L2-only, with an L2 eviction-priority policy (for streamed data).
-__device__ __forceinline__ void cp_async_16_hint(void* dst, const void* src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 ::"r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
-}
-__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
+// Per-thread asynchronous 4-byte copy (for scale and bias rows that are not
+// 16-byte multiples).
 __device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
