@@ -151,6 +151,36 @@ def test_one_hot_gives_dequantized_weight(bits, group):
         assert np.array_equal(y[:, n], expect)       # s*q needs <= 19 bits: exact in float64
 
 
+@pytest.mark.parametrize("bits,group", [(2, 32), (3, 64), (4, 32), (4, 64), (5, 32), (6, 64), (8, 32), (8, 64)])
+def test_dequant_matches_definition_row_by_row(bits, group):
+    """dequant_f64 against W[n,k] = s[n, k//group] * q[n,k] + b[n, k//group]
+    written here with numpy's binary16 and codes packed by the test's own
+    packer; then against the columns of qmm_f64 on identity activations (the
+    one-hot row k of x picks column k of W). Rows have distinct scales, so a
+    wrong row offset into the scales or biases fails."""
+    o = _oracle()
+    rng = np.random.default_rng(41 * bits + group)
+    N = 7
+    K = 4 * group
+    while (K * bits) % 32:
+        K += group
+    G = K // group
+    codes = rng.integers(0, 1 << bits, size=(N, K)).astype(np.uint8)
+    words = pack_rows(codes, bits)
+    s = (rng.uniform(0.002, 0.5, size=(N, G)) * (1 + np.arange(N))[:, None]).astype(np.float16)
+    b = rng.uniform(-3, 3, size=(N, G)).astype(np.float16)
+    W = o.dequant_f64(words, s.view(np.uint16), b.view(np.uint16), K, N, bits, group)
+    assert W.shape == (N, K)
+    gi = np.arange(K) // group
+    for n in range(N):
+        expect = s[n, gi].astype(np.float64) * codes[n].astype(np.float64) + b[n, gi].astype(np.float64)
+        assert np.array_equal(W[n], expect), n      # s*q needs <= 19 bits: exact in float64
+    x = np.zeros((K, K), dtype=np.uint16)
+    x[np.arange(K), np.arange(K)] = 0x3F80           # bfloat16 1.0 on the diagonal
+    y = o.qmm_f64(x, words, s.view(np.uint16), b.view(np.uint16), K, N, bits, group)
+    assert np.array_equal(y, W.T)
+
+
 # ---------------------------------------------------------------------------
 # Exact special case and brute force with rational arithmetic
 # ---------------------------------------------------------------------------
