@@ -238,10 +238,10 @@ int qmm_plan_error(const qmm_plan_t* p, uint32_t* flags);
  * directly (QMM_OUT_F32 or QMM_OUT_BF16) and splits fixed at 1. The per-call
  * activation staging lives in a static device array of
  * QMM_NOALLOC_SCRATCH_BYTES; a call whose staging would not fit returns
- * QMM_ERR_SCRATCH_LIMIT before touching the device (with 9..16 rows the
- * largest K is 114688 for 4/5/6-bit codes in groups of 32, 122368 in groups of
- * 64, and 61184 / 62976 for 8-bit codes; with 1..8 rows about twice that). Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
- * library routine.
+ * QMM_ERR_SCRATCH_LIMIT before touching the device. The staging size does not
+ * depend on the code width: with 9..16 rows the largest K is 114688 in groups
+ * of 32 and 122368 in groups of 64; with 1..8 rows 229632 and 244736. Nothing
+ * is allocated: no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * The first call on a device (with that device current) looks up the
  * scratch's device address and sets the kernels' shared-memory limit; make

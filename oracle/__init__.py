@@ -12,6 +12,8 @@ builds it with g++ on first use and exposes numpy-facing wrappers:
 * ``dequant_f64`` -- ``W = s*q + b`` in float64.
 * ``qmm_f64`` / ``qmm_f64_cols`` -- the definition ``y = x @ W.T`` in float64,
   k ascending (all columns, or a chosen subset).
+* ``qmm_swiglu_f64`` / ``qmm_swiglu_f64_cols`` -- silu(qmm(x, gate)) * qmm(x, up)
+  in float64 (all columns, or a chosen subset).
 * ``qmm_spbxs_f64`` -- the dequant-after-dot form ``sum_g s*P + b*XS``
   ("C += s*P + b*XS", vmlx-swift PR #565, LaneQMM commit), used only to check
   that it equals the definition.
@@ -66,11 +68,13 @@ def _load():
             lib.oracle_qmm_f64_cols.argtypes = [vp, i64, vp, vp, vp, i64, i64, i32, i32, vp, i64, vp]
             lib.oracle_qmm_spbxs_f64.argtypes = [vp, i64, vp, vp, vp, i64, i64, i32, i32, vp]
             lib.oracle_qmm_swiglu_f64.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, vp]
+            lib.oracle_qmm_swiglu_f64_cols.argtypes = [vp, i64, vp, vp, vp, vp, vp, vp, i64, i64, i32, i32, vp,
+                                                       i64, vp]
             lib.oracle_max_threads.restype = ctypes.c_int
             lib.oracle_set_threads.argtypes = [ctypes.c_int]
             for name in ("oracle_decode_bitwise", "oracle_decode_wordwise", "oracle_dequant_f64",
                          "oracle_qmm_f64", "oracle_qmm_f64_cols", "oracle_qmm_spbxs_f64",
-                         "oracle_qmm_swiglu_f64"):
+                         "oracle_qmm_swiglu_f64", "oracle_qmm_swiglu_f64_cols"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -164,6 +168,20 @@ def qmm_swiglu_f64(x_bf16, words_gate, scales_gate, biases_gate, words_up, scale
     y = np.empty((M, N), dtype=np.float64)
     _check(_load().oracle_qmm_swiglu_f64(_p(x), M, _p(wg), _p(sg), _p(bg), _p(wu), _p(su), _p(bu), K, N, bits,
                                          group, _p(y)), "qmm_swiglu_f64")
+    return y
+
+
+def qmm_swiglu_f64_cols(x_bf16, words_gate, scales_gate, biases_gate, words_up, scales_up, biases_up,
+                        K: int, N: int, bits: int, group: int, cols) -> np.ndarray:
+    """qmm_swiglu_f64 for the listed output columns only; returns [M, len(cols)]."""
+    x = _c(x_bf16, np.uint16).reshape(-1, K)
+    wg, sg, bg = _c(words_gate, np.uint32), _c(scales_gate, np.uint16), _c(biases_gate, np.uint16)
+    wu, su, bu = _c(words_up, np.uint32), _c(scales_up, np.uint16), _c(biases_up, np.uint16)
+    cols = _c(cols, np.int64).reshape(-1)
+    M = x.shape[0]
+    y = np.empty((M, cols.size), dtype=np.float64)
+    _check(_load().oracle_qmm_swiglu_f64_cols(_p(x), M, _p(wg), _p(sg), _p(bg), _p(wu), _p(su), _p(bu), K, N,
+                                              bits, group, _p(cols), cols.size, _p(y)), "qmm_swiglu_f64_cols")
     return y
 
 

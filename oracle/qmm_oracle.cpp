@@ -285,6 +285,27 @@ int oracle_qmm_swiglu_f64(const uint16_t* x_bf16, int64_t M, const uint32_t* wor
     return 0;
 }
 
+// The same for the listed output columns only (ncols of them; y is [M, ncols]),
+// from the column-subset form of the plain definition.
+int oracle_qmm_swiglu_f64_cols(const uint16_t* x_bf16, int64_t M, const uint32_t* words_gate,
+                               const uint16_t* scales_gate, const uint16_t* biases_gate,
+                               const uint32_t* words_up, const uint16_t* scales_up, const uint16_t* biases_up,
+                               int64_t K, int64_t N, int bits, int group, const int64_t* cols, int64_t ncols,
+                               double* y) {
+    if (check_qmm(M, K, N, bits, group) || cols == nullptr || ncols < 0) return 1;
+    std::vector<double> g((size_t)(M * ncols)), u((size_t)(M * ncols));
+    if (oracle_qmm_f64_cols(x_bf16, M, words_gate, scales_gate, biases_gate, K, N, bits, group, cols, ncols,
+                            g.data()))
+        return 1;
+    if (oracle_qmm_f64_cols(x_bf16, M, words_up, scales_up, biases_up, K, N, bits, group, cols, ncols, u.data()))
+        return 1;
+    for (int64_t i = 0; i < M * ncols; ++i) {
+        const double v = g[(size_t)i];
+        y[i] = v / (1.0 + std::exp(-v)) * u[(size_t)i];
+    }
+    return 0;
+}
+
 // Number of threads the parallel regions above use (for reporting).
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -425,3 +425,39 @@ def test_swiglu_brute_force_tiny():
         for n in range(N):
             want = g[m, n] / (1.0 + math.exp(-g[m, n])) * u[m, n]
             assert math.isclose(y[m, n], want, rel_tol=1e-11, abs_tol=1e-12)
+
+
+def test_swiglu_column_subset():
+    """The column-subset form on a tiny case, columns out of order and repeated,
+    against a triple loop written here (dequantize, dot, silu through tanh),
+    and bitwise equal to the full form's columns on a larger case."""
+    import datagen
+    o = _oracle()
+    bits, group, K, N, M = 3, 64, 128, 4, 3
+    a = datagen.gen_qmm(51, M, K, N, bits, group)
+    c = datagen.gen_qmm(52, M, K, N, bits, group)
+    cols = np.array([3, 0, 3, 1], dtype=np.int64)
+    y = o.qmm_swiglu_f64_cols(a.x, a.words[0], a.scales[0], a.biases[0], c.words[0], c.scales[0], c.biases[0],
+                              K, N, bits, group, cols)
+    assert y.shape == (M, cols.size)
+    xs = (a.x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    gi = np.arange(K) // group
+
+    def proj(inp, n):
+        codes = inp.words[0][n]
+        q = np.array([(int(sum(int(w) << (32 * i) for i, w in enumerate(codes))) >> (k * bits)) & ((1 << bits) - 1)
+                      for k in range(K)], dtype=np.float64)
+        s = inp.scales[0].view(np.float16)[n, gi].astype(np.float64)
+        b = inp.biases[0].view(np.float16)[n, gi].astype(np.float64)
+        return xs @ (s * q + b)
+
+    for j, n in enumerate(cols):
+        g, u = proj(a, n), proj(c, n)
+        want = np.array([_silu_tanh(v) for v in g]) * u
+        assert np.allclose(y[:, j], want, rtol=1e-12, atol=1e-14 * np.max(np.abs(want)))
+    K2, N2 = 512, 40
+    a2 = datagen.gen_qmm(53, 2, K2, N2, 4, 32)
+    c2 = datagen.gen_qmm(54, 2, K2, N2, 4, 32)
+    args = (a2.x, a2.words[0], a2.scales[0], a2.biases[0], c2.words[0], c2.scales[0], c2.biases[0], K2, N2, 4, 32)
+    cols2 = np.array([39, 7, 0, 21], dtype=np.int64)
+    assert np.array_equal(o.qmm_swiglu_f64_cols(*args, cols2), o.qmm_swiglu_f64(*args)[:, cols2])
