@@ -9,6 +9,14 @@ Inputs are seeded synthetic data (datagen), resident in HBM before timing.
 Metric: effective HBM GB/s = (packed codes + fp16 scales + fp16 biases + bf16 x
 + bf16 y) bytes / time, plus us/call and GB/s per M.
 
+The same line carries `per_config`: us/call, GB/s and the fraction of the
+measured HBM peak for the other named configurations, each over rotating device
+copies of its weights larger than L2 and timed by CUDA-graph replay: pr1_ref
+(M=1, 2048 x 2048, 4-bit g64, fp32 out; also with direct stream launches),
+down_longk (17408 -> 5120, 4-bit g64, splits 1/2/4/8/automatic x M 1/8/16),
+mixed_widths (5120 -> 6144, 5/6/8-bit g32, M=8) and banked (36 banks of
+2048 -> 8192, 4-bit g64, M 1 and 16, per bank set).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qmm|reference]
 
 --impl reference times the CPU oracle (float64 C++) on the same workload (a
@@ -165,6 +173,149 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
                 "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Every named configuration, timed the same way (a JSON object in the line)
+# ---------------------------------------------------------------------------
+L2_BYTES = 129 * 2 ** 20
+
+
+def _time_step(step, reps, stream, graph=True, passes=3):
+    """Seconds per step(): warm-up, then (optionally) one CUDA-graph capture of
+    step() replayed `reps` times; the fastest of `passes` timed passes."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(passes):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            (g.replay() if g is not None else step())
+            e0.record(stream)
+            for _ in range(reps):
+                (g.replay() if g is not None else step())
+            e1.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) / 1e3 / reps)
+    del g
+    return best
+
+
+def _dev_copies(name, bits, M, banks=1, min_bytes=3 * L2_BYTES):
+    """x on the device and enough device copies of the workload's weights
+    (clones of one seeded copy per bank) that one rotation exceeds `min_bytes`."""
+    import torch
+    wl = datagen.WORKLOADS[name]
+    K, N, group = wl["K"], wl["N"], wl["group"]
+    inp = datagen.gen_qmm(datagen.workload_seed(name) + bits, M, K, N, bits, group, banks=banks)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = torch.from_numpy(inp.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    base = [(torch.from_numpy(inp.words[i].view(np.int32)).to(dev),
+             torch.from_numpy(inp.scales[i].view(np.int16)).to(dev).view(torch.float16),
+             torch.from_numpy(inp.biases[i].view(np.int16)).to(dev).view(torch.float16)) for i in range(banks)]
+    per_set = banks * algorithmic_bytes(0, K, N, bits, group, 0)
+    sets = max(1, -(-min_bytes // per_set))
+    copies = [base] + [[tuple(t.clone() for t in bk) for bk in base] for _ in range(sets - 1)]
+    return x, copies, (K, N, group)
+
+
+def run_per_config(q, peaks, stream):
+    """us/call (or per bank set), effective GB/s and fraction of the measured HBM
+    peak for every named configuration other than the headline's."""
+    import torch
+    peak = peaks["hbm_gbs"]
+    res = {}
+
+    def entry(sec, nbytes, extra=None):
+        d = {"us": round(sec * 1e6, 3), "gbs": round(nbytes / sec / 1e9, 1), "frac": round(nbytes / sec / 1e9 / peak, 4)}
+        if extra:
+            d.update(extra)
+        return d
+
+    # pr1_ref: M=1, 2048 x 2048, 4-bit g64, fp32 out; direct stream launches and graph replay
+    x, copies, (K, N, group) = _dev_copies("pr1_ref", 4, 1)
+    plan = q.Plan(K, N, 4, group, max_M=1, out_dtype="f32", splits=0)
+    out = torch.empty((1, N), dtype=torch.float32, device=x.device)
+
+    def step_pr1():
+        for c in copies:
+            q.forward(plan, x, c[0][0], c[0][1], c[0][2], out, stream=stream)
+    nb = algorithmic_bytes(1, K, N, 4, group, 4)
+    reps = max(5, 2000 // len(copies))
+    sg = _time_step(step_pr1, reps, stream, graph=True) / len(copies)
+    sd = _time_step(step_pr1, reps, stream, graph=False) / len(copies)
+    res["pr1_ref"] = {"workload": f"M=1 K={K} N={N} 4-bit g{group} f32 out", "splits": plan.info()["splits"],
+                      "copies": len(copies), "graph": entry(sg, nb), "stream": entry(sd, nb)}
+    assert plan.error_flags() == 0
+    del copies, plan
+
+    # down_longk: 17408 -> 5120, 4-bit g64, bf16 out, splits 1/2/4/8/auto x M 1/8/16
+    x, copies, (K, N, group) = _dev_copies("down_longk", 4, 16)
+    dl = {"workload": f"K={K} N={N} 4-bit g{group} bf16 out", "copies": len(copies)}
+    for splits in (1, 2, 4, 8, 0):
+        plan = q.Plan(K, N, 4, group, max_M=16, out_dtype="bf16", splits=splits)
+        row = {"splits_used": plan.info()["splits"]}
+        for M in (1, 8, 16):
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+
+            def step_dl():
+                for c in copies:
+                    q.forward(plan, x[:M], c[0][0], c[0][1], c[0][2], out, stream=stream)
+            sec = _time_step(step_dl, max(5, 400 // len(copies)), stream) / len(copies)
+            row[str(M)] = entry(sec, algorithmic_bytes(M, K, N, 4, group, 2))
+        assert plan.error_flags() == 0
+        dl["auto" if splits == 0 else f"splits={splits}"] = row
+        del plan
+    res["down_longk"] = dl
+    del copies
+
+    # mixed widths: 5120 -> 6144, 5/6/8-bit g32, M=8, bf16 out, automatic splits
+    mw = {}
+    for bits in (5, 6, 8):
+        x, copies, (K, N, group) = _dev_copies("mixed_widths", bits, 8)
+        plan = q.Plan(K, N, bits, group, max_M=8, out_dtype="bf16", splits=0)
+        out = torch.empty((8, N), dtype=torch.bfloat16, device=x.device)
+
+        def step_mw():
+            for c in copies:
+                q.forward(plan, x, c[0][0], c[0][1], c[0][2], out, stream=stream)
+        sec = _time_step(step_mw, max(5, 400 // len(copies)), stream) / len(copies)
+        mw[f"{bits}-bit"] = entry(sec, algorithmic_bytes(8, K, N, bits, group, 2),
+                                  {"splits": plan.info()["splits"], "copies": len(copies)})
+        assert plan.error_flags() == 0
+        del copies, plan
+    res["mixed_widths"] = {"workload": "M=8 K=5120 N=6144 g32 bf16 out", **mw}
+
+    # banked: 36 x (2048 -> 8192), 4-bit g64, shared x, M 1 and 16, per bank set
+    x, sets, (K, N, group) = _dev_copies("banked", 4, 16, banks=36, min_bytes=2 * L2_BYTES)
+    B = 36
+    plan = q.Plan(K, N, 4, group, max_M=16, out_dtype="bf16", splits=0, max_banks=B)
+    bk = {"workload": f"{B} banks x (K={K} N={N} 4-bit g{group}) shared x, bf16 out", "bank_sets": len(sets),
+          "splits": plan.info()["splits"]}
+    for M in (1, 16):
+        outs = [torch.empty((M, N), dtype=torch.bfloat16, device=x.device) for _ in range(B)]
+
+        def step_bk():
+            for st in sets:
+                q.forward_banked(plan, x[:M], [c[0] for c in st], [c[1] for c in st], [c[2] for c in st], outs,
+                                 stream=stream)
+        sec = _time_step(step_bk, max(5, 100 // len(sets)), stream) / len(sets)
+        bk[str(M)] = entry(sec, B * algorithmic_bytes(M, K, N, 4, group, 2), {"unit": "per bank set"})
+    assert plan.error_flags() == 0
+    res["banked"] = bk
+    del sets, plan
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -327,6 +478,12 @@ def run_gpu(args, ws, rank, local):
     if flags != 0:
         raise RuntimeError(f"kernel reported a bounded-wait timeout (flags={flags})")
 
+    per_config = None
+    if not args.no_per_config:
+        del W, S, B
+        torch.cuda.empty_cache()
+        per_config = run_per_config(q, peaks, stream)
+
     if rank != 0:
         return
     traffic = None
@@ -353,6 +510,7 @@ def run_gpu(args, ws, rank, local):
                    "launch": "cuda_graph" if graphed else "direct", "splits": info["splits"],
                    "stages": info["stages"], "parallelism": f"replicas x{ws}", "accumulate": "fp32"},
         "per_M": per_m,
+        "per_config": per_config,
         "roofline": {"bound": "hbm", "achieved": round(value / ws, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(value / ws / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "peak_source": peaks["source"], "kernel": "qmm_main_kernel (timed with its staging kernel)"},
@@ -601,6 +759,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qmm", "reference"], default="qmm")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of CUDA graph replay")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration timings (pr1_ref, down_longk, mixed_widths, banked)")
     ap.add_argument("--ncu-case", type=int, default=0, metavar="M",
                     help="run a small untimed profiling case with M rows and exit")
     ap.add_argument("--case-workload", default=WORKLOAD, choices=sorted(datagen.WORKLOADS))
