@@ -2,8 +2,6 @@
 // dispatch. Declarations and the contract are in include/qmm.h.
 #include <cuda_runtime.h>
 
-#include <cudaTypedefs.h>
-
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -11,7 +9,7 @@
 #include <unordered_map>
 
 #include "../../include/qmm.h"
-#include "qmm_kernels.cuh"
+#include "qmm_host.h"
 
 using namespace qmmk;
 
@@ -30,7 +28,6 @@ struct qmm_plan {
     size_t ws_bytes;
     bool owns_ws;
     uint32_t* err;       // device error word (start of the workspace)
-    uint8_t* xprep;
     float* partial;
     // TMA tensor maps already encoded for a given base pointer (weights, scales, biases)
     std::unordered_map<const void*, CUtensorMap> wmaps, smaps, bmaps;
@@ -39,8 +36,6 @@ struct qmm_plan {
 namespace {
 
 constexpr size_t kErrBytes = 256;
-
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int chunks_of(const qmm_desc* d) {
     const int64_t G = d->K / d->group;
@@ -56,47 +51,12 @@ int splits_cap(const qmm_desc* d) {
     return c;
 }
 
-// Automatic K-slice count from a per-CTA cost model, fitted on GB300 to the
-// 4-bit group-64 K=17408 N=5120 projection over 1, 2, 4 and 8 slices: a CTA
-// pays, per row block of up to 128 rows, one pass over its slice's chunks
-// (chunk bytes at about 28 GB/s per SM) plus about 2 us of restart, and
-// slicing adds about 3.7 us for the partial sums and their reduce. The work is
-// cut evenly over (bank, slice, row) space, so when the CTA count is not a
-// multiple of the bank-slice segments some CTA ranges straddle two segments
-// and pay one more row block. Slices keep at least 2 chunks.
 int auto_splits(const qmm_desc* d, int num_sms) {
-    const int C = chunks_of(d);
-    const double chunk_us = kTN * (chunk_row_bytes(d->bits, d->group) + 4.0 * kGPC) / 28e3;
-    const double row_block_us = 2.0;
-    const double split_us = 3.7;
-    const int64_t banks = d->max_banks > 0 ? d->max_banks : 1;
-    int best = 1;
-    double best_cost = 0.0;
-    for (int s = 1; s <= splits_cap(d); ++s) {
-        if (s > 1 && C / s < 2) break;
-        const int64_t rows_total = banks * s * d->N;
-        int64_t ctas = (rows_total + kSlab - 1) / kSlab;
-        if (ctas > num_sms) ctas = num_sms;
-        const int64_t rows_per_cta = (rows_total + ctas - 1) / ctas;
-        int64_t blocks = (rows_per_cta + kTN - 1) / kTN;
-        if (ctas % (banks * s) != 0) ++blocks;
-        const int per_slice = (C + s - 1) / s;
-        const double cost = blocks * (per_slice * chunk_us + row_block_us) + (s > 1 ? split_us : 0.0);
-        if (s == 1 || cost < best_cost) {
-            best = s;
-            best_cost = cost;
-        }
-    }
-    return best;
+    return auto_split_count(d->K, d->N, d->bits, d->group, d->max_banks > 0 ? d->max_banks : 1, num_sms,
+                            splits_cap(d));
 }
 
 int mb_index(int M) { return M > 8 ? 1 : 0; }
-int max_mb(const qmm_desc* d) { return d->max_M > 8 ? 16 : 8; }
-
-size_t xprep_region_bytes(const qmm_desc* d) {
-    return static_cast<size_t>(chunks_of(d)) *
-           static_cast<size_t>(xprep_chunk_bytes(d->bits, d->group, max_mb(d)));
-}
 
 size_t partial_region_bytes(const qmm_desc* d, int splits) {
     // unsliced plans with two or more banks keep room for the fused gate/up
@@ -107,75 +67,6 @@ size_t partial_region_bytes(const qmm_desc* d, int splits) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-cudaError_t configure(int bits, int group, int mb, int smem) {
-    switch (bits) {
-        case 2: return configure_kernels<2>(group, mb, smem);
-        case 3: return configure_kernels<3>(group, mb, smem);
-        case 4: return configure_kernels<4>(group, mb, smem);
-        case 5: return configure_kernels<5>(group, mb, smem);
-        case 6: return configure_kernels<6>(group, mb, smem);
-        case 8: return configure_kernels<8>(group, mb, smem);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-cudaError_t launch(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,
-                   const MainParams<kMaxBanks>* banked, const MainParams<2>* fused = nullptr) {
-    switch (bits) {
-        case 2: return launch_forward<2>(group, L, single, banked, fused);
-        case 3: return launch_forward<3>(group, L, single, banked, fused);
-        case 4: return launch_forward<4>(group, L, single, banked, fused);
-        case 5: return launch_forward<5>(group, L, single, banked, fused);
-        case 6: return launch_forward<6>(group, L, single, banked, fused);
-        case 8: return launch_forward<8>(group, L, single, banked, fused);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-// cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// Packed codes as uint8 [N][row_bytes]; box kTN rows x W bytes with the W-byte swizzle.
-bool encode_weights(const struct qmm_plan* p, const void* w, CUtensorMap* out) {
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr) return false;
-    const int W = weight_box_width(p->d.bits, p->d.group);
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->d.K * p->d.bits / 8), static_cast<cuuint64_t>(p->d.N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->d.K * p->d.bits / 8)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(W), static_cast<cuuint32_t>(kTN)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapSwizzle sw = W == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
-                                           : (W == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Scales or biases as uint16 [N][G]; box kTN rows x 8 values, unswizzled.
-bool encode_sb(const struct qmm_plan* p, const void* a, CUtensorMap* out) {
-    auto enc = tensor_map_encoder();
-    if (enc == nullptr) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->G), static_cast<cuuint64_t>(p->d.N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->G) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGPC), static_cast<cuuint32_t>(kTN)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Cached lookup; the cache is cleared when it grows past a few thousand pointers.
 bool tensor_map_for(struct qmm_plan* p, std::unordered_map<const void*, CUtensorMap>& cache, const void* ptr, bool weights,
                     CUtensorMap* out) {
@@ -185,7 +76,9 @@ bool tensor_map_for(struct qmm_plan* p, std::unordered_map<const void*, CUtensor
         return true;
     }
     CUtensorMap m;
-    if (!(weights ? encode_weights(p, ptr, &m) : encode_sb(p, ptr, &m))) return false;
+    if (!(weights ? encode_weight_map(ptr, p->d.K, p->d.N, p->d.bits, p->d.group, &m)
+                  : encode_sb_map(ptr, p->G, p->d.N, &m)))
+        return false;
     if (cache.size() >= 4096) cache.clear();
     cache.emplace(ptr, m);
     *out = m;
@@ -229,7 +122,7 @@ int qmm_validate_desc(const qmm_desc* d) {
 
 size_t qmm_workspace_bytes(const qmm_desc* d) {
     if (qmm_validate_desc(d) != QMM_OK) return 0;
-    return kErrBytes + align_up(xprep_region_bytes(d), 256) + partial_region_bytes(d, splits_cap(d));
+    return kErrBytes + partial_region_bytes(d, splits_cap(d));
 }
 
 int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_bytes) {
@@ -263,16 +156,14 @@ int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_by
     }
     for (int i = 0; i < nmb; ++i) {
         const int mb = i == 0 ? 8 : 16;
-        const int sb = stage_bytes(d->bits, d->group, mb);
-        int st = (optin - 2048 - reduce_scratch_bytes(mb)) / (sb + 16);
-        if (st > kMaxStages) st = kMaxStages;
+        const int st = stages_for(d->bits, d->group, mb, optin);
         if (st < 2) {
             delete p;
             return QMM_ERR_UNSUPPORTED;
         }
         p->stages[i] = st;
-        p->smem[i] = main_smem_bytes(d->bits, d->group, mb, st);
-        if (configure(d->bits, d->group, mb, p->smem[i]) != cudaSuccess) {
+        p->smem[i] = main_smem_bytes(d->bits, d->group, mb);
+        if (configure_format(d->bits, d->group, mb, p->smem[i]) != cudaSuccess) {
             delete p;
             return QMM_ERR_CUDA;
         }
@@ -293,8 +184,7 @@ int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_by
         p->owns_ws = false;
     }
     p->err = reinterpret_cast<uint32_t*>(p->ws);
-    p->xprep = p->ws + kErrBytes;
-    p->partial = reinterpret_cast<float*>(p->ws + kErrBytes + align_up(xprep_region_bytes(d), 256));
+    p->partial = reinterpret_cast<float*>(p->ws + kErrBytes);
     if (cudaMemsetAsync(p->ws, 0, kErrBytes, 0) != cudaSuccess || cudaStreamSynchronize(0) != cudaSuccess) {
         if (p->owns_ws) cudaFree(p->ws);
         delete p;
@@ -329,7 +219,7 @@ int qmm_check_forward_args(const qmm_desc* d, const void* x_bf16, int M, int n_b
     if (packed_w == nullptr || scales_f16 == nullptr || biases_f16 == nullptr || out == nullptr)
         return QMM_ERR_INVALID_ARG;
     if (M == 0) return QMM_OK;
-    if (x_bf16 == nullptr || !aligned(x_bf16, 2)) return QMM_ERR_INVALID_ARG;
+    if (x_bf16 == nullptr || !aligned(x_bf16, 16)) return QMM_ERR_INVALID_ARG;
     const size_t sb_align = ((d->K / d->group) % 8 == 0) ? 16 : 4;
     const size_t out_align = d->out_dtype == QMM_OUT_F32 ? 4 : 2;
     for (int i = 0; i < n_banks; ++i) {
@@ -361,39 +251,35 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
 
     MainHeader h;
     std::memset(&h, 0, sizeof(h));
-    h.xprep = p->xprep;
+    h.x = static_cast<const uint16_t*>(x_bf16);
     h.partial = p->partial;
     h.err = p->err;
     h.N = N;
     h.K = K;
-    h.row_bytes = K * bits / 8;
     h.G = p->G;
     h.C = p->C;
     h.splits = p->splits;
     h.M = M;
-    h.stages = p->stages[mi];
     h.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
     h.sb_tma = (p->G % 8 == 0) ? 1 : 0;
-    h.sb_vec16 = h.sb_tma;
     h.unpack_magic = kF16x2_1024;
     h.banks = n_banks;
-    h.swiglu = swiglu ? 1 : 0;
     h.gate = swiglu ? p->partial : nullptr;
-    h.xprep_bytes = static_cast<int64_t>(p->C) * xprep_chunk_bytes(bits, group, mi == 0 ? 8 : 16);
     h.rows_total = static_cast<int64_t>(swiglu ? 1 : n_banks) * p->splits * N;
 
     int64_t ctas = (h.rows_total + kSlab - 1) / kSlab;
     if (ctas > p->num_sms) ctas = p->num_sms;
     LaunchCfg L;
-    L.x = static_cast<const uint16_t*>(x_bf16);
-    L.M = M;
     L.mb = mi == 0 ? 8 : 16;
     L.ctas = static_cast<int>(ctas);
     L.smem = p->smem[mi];
     L.stream = st;
 
+    CUtensorMap xmap;
+    if (!encode_x_map(x_bf16, M, K, group, L.mb, &xmap)) return QMM_ERR_CUDA;
     auto fill = [&](auto& mp) -> bool {
         mp.h = h;
+        mp.tmx = xmap;
         for (int i = 0; i < n_banks; ++i) {
             mp.bank[i].w = packed_w[i];
             mp.bank[i].s = scales_f16[i];
@@ -412,17 +298,17 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
         MainParams<2> mp2;
         std::memset(&mp2, 0, sizeof(mp2));
         if (!fill(mp2)) return QMM_ERR_CUDA;
-        le = launch(bits, group, L, nullptr, nullptr, &mp2);
+        le = launch_format(bits, group, L, nullptr, nullptr, &mp2);
     } else if (n_banks == 1) {
         MainParams<1> mp1;
         std::memset(&mp1, 0, sizeof(mp1));
         if (!fill(mp1)) return QMM_ERR_CUDA;
-        le = launch(bits, group, L, &mp1, nullptr);
+        le = launch_format(bits, group, L, &mp1, nullptr, nullptr);
     } else {
         static thread_local MainParams<kMaxBanks> mpb;   // 25 KB: kept off the stack
         std::memset(&mpb, 0, sizeof(mpb));
         if (!fill(mpb)) return QMM_ERR_CUDA;
-        le = launch(bits, group, L, nullptr, &mpb);
+        le = launch_format(bits, group, L, nullptr, &mpb, nullptr);
     }
     if (le != cudaSuccess) return QMM_ERR_CUDA;
 

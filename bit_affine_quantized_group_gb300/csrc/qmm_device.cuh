@@ -76,17 +76,108 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait on a phase parity; on timeout sets `code` in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
+// As mbar_try_wait, but the thread may stay suspended (without issuing) for up
+// to `hint_ns` nanoseconds while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a phase parity; on timeout sets `code` in *err and returns
+// false. The first test is inline; the retry loop is out of line (it runs only
+// when the phase has not completed yet).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
+    // each try sleeps until the phase completes or 20 us pass, so a waiting warp
+    // leaves the issue slots to the others
     const unsigned long long t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    for (uint32_t n = 1;; ++n) {
+        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+        // after any recorded failure the kernel stops waiting (its output is then
+        // incomplete; the host sees the error word) so that no warp spends the
+        // limit again; the word is read only every 64 tries, off the path of a
+        // wait that ends soon
+        if ((n & 63u) == 0 &&
+            (*reinterpret_cast<volatile uint32_t*>(err) & (kErrFullWait | kErrEmptyWait | kErrDrainWait)))
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(err, code);
             return false;
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, code);
+}
+// As mbar_wait, for a warp that runs ahead of the one it waits for (a
+// producer refilling a slot, a stager waiting for a slot to empty): between
+// tries it sleeps about `ns` nanoseconds, leaving the issue slots to the warps
+// on the critical path.
+static __device__ __noinline__ bool mbar_wait_sleep_slow(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                                         uint32_t ns) {
+    const unsigned long long t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        __nanosleep(ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((n & 63u) == 0 &&
+            (*reinterpret_cast<volatile uint32_t*>(err) & (kErrFullWait | kErrEmptyWait | kErrDrainWait)))
+            return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, code);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                                uint32_t ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_sleep_slow(bar, parity, err, code, ns);
+}
+// Bounded wait for this warp's own copies still in flight after a failure
+// (before the CTA exits): unlike mbar_wait it waits even when an error is
+// already recorded; on timeout it sets kErrDrainWait and returns false.
+static __device__ __noinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    const unsigned long long t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrDrainWait);
+            return false;
+        }
+    }
+}
+
+// ---- paired fp32 arithmetic ---------------------------------------------------
+// One instruction for two lanes of fp32 work; each half is rounded exactly as
+// the scalar operation (fmaf, +, *) would round it.
+__device__ __forceinline__ void fma_x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                       float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul_x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // ---- copies -----------------------------------------------------------------
@@ -109,6 +200,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
+// 3-D TMA tile load, as tma_load_2d with coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -128,6 +227,81 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // (the arrival is pre-counted in the barrier's initial count).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before its
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---- shared-memory loads ---------------------------------------------------
+// Four 8x8 b16 matrices; lane l gives the row address of row (l & 7) of
+// matrix (l >> 3) (16-byte aligned), and receives in register i the 32-bit
+// word (l & 3) of row (l >> 2) of matrix i.
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& d0, uint32_t& d1, uint32_t& d2, uint32_t& d3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(addr));
+}
+// Shared loads at base + a compile-time byte offset ([reg + imm] addressing).
+template <int OFF>
+__device__ __forceinline__ uint4 lds128_at(uint32_t base) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4 + %5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(base), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 lds64_at(uint32_t base) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2 + %3];" : "=r"(v.x), "=r"(v.y) : "r"(base), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t lds32_at(uint32_t base) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1 + %2];" : "=r"(v) : "r"(base), "n"(OFF));
+    return v;
+}
+template <int OFF>
+__device__ __forceinline__ void ldmatrix_x4_at(uint32_t base, uint32_t& d0, uint32_t& d1, uint32_t& d2, uint32_t& d3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4 + %5];"
+                 : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+                 : "r"(base), "n"(OFF));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Per-half max of |a|, |b| of two bfloat16 pairs (the sign bits of the result
+// are the xor of the operands' and are masked by the caller).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // ---- tensor-core MMA (warp level) -------------------------------------------
@@ -163,7 +337,11 @@ constexpr uint32_t kF16x2_1024 = 0x64006400u;
 // three-input logic op takes a single immediate, so with both the mask and the
 // pattern as literals every (w & mask) | pattern would compile to two ops.
 
-// Slot tables: which of the lane's 8 codes, and its mantissa shift j.
+// Slot tables: which code of the k32 block lane t holds in register r, half
+// h, and its mantissa shift j. Lane t holds codes 8t .. 8t + 7 of the block,
+// except with 8-bit codes, where it holds codes 4t .. 4t + 3 and
+// 16 + 4t .. 16 + 4t + 3 (word t of each 16-byte half of the block's row, as
+// ldmatrix delivers them).
 QMM_HD constexpr int slot_code(int bits, int r, int h) {
     return bits == 2 ? r + 4 * h
          : bits == 3 ? (r < 3 ? (h == 0 ? r : r + 5) : 3 + h)
@@ -172,6 +350,9 @@ QMM_HD constexpr int slot_code(int bits, int r, int h) {
          : bits == 5 ? (h == 0 ? r : r + 4)
          : /* 6 */     (r < 3 ? (h == 0 ? r : r + 3) : 6 + h);
 }
+QMM_HD constexpr int block_code(int bits, int t, int r, int h) {
+    return bits == 8 ? 4 * t + 16 * (r >> 1) + (r & 1) + 2 * h : 8 * t + slot_code(bits, r, h);
+}
 QMM_HD constexpr int slot_shift(int bits, int r, int h) {
     return bits == 2 ? 2 * r
          : bits == 3 ? ((r < 3 && h == 0) ? 1 : 0)
@@ -179,15 +360,6 @@ QMM_HD constexpr int slot_shift(int bits, int r, int h) {
          : bits == 8 ? 0
          : bits == 5 ? (h == 0 ? 0 : 4)
          : /* 6 */     ((r < 3 && h == 1) ? 2 : 0);
-}
-// Shift j of the lane's code i (the inverse view of the tables).
-QMM_HD constexpr int code_shift(int bits, int i) {
-    return bits == 2 ? 2 * (i & 3)
-         : bits == 3 ? (i < 3 ? 1 : 0)
-         : bits == 4 ? ((i & 1) ? 4 : 0)
-         : bits == 8 ? 0
-         : bits == 5 ? (i < 4 ? 0 : 4)
-         : /* 6 */     ((i >= 3 && i <= 5) ? 2 : 0);
 }
 
 // 4-bit: one word holds the lane's 8 codes, nibble i = code i.
@@ -199,13 +371,14 @@ __device__ __forceinline__ void unpack4(uint32_t w, uint32_t (&r)[4], uint32_t m
     r[3] = (w8 & 0x00F000F0u) | magic;         // c3, c7
 }
 
-// 8-bit: two words hold the lane's 8 codes, byte i = code i.
+// 8-bit: two words hold the lane's 8 codes, byte i of w0 = code 4t + i and
+// byte i of w1 = code 16 + 4t + i.
 __device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t (&r)[4],
                                         uint32_t magic = kF16x2_1024) {
-    r[0] = (w0 & 0x00FF00FFu) | magic;         // c0, c2
-    r[1] = ((w0 >> 8) & 0x00FF00FFu) | magic;  // c1, c3
-    r[2] = (w1 & 0x00FF00FFu) | magic;         // c4, c6
-    r[3] = ((w1 >> 8) & 0x00FF00FFu) | magic;  // c5, c7
+    r[0] = (w0 & 0x00FF00FFu) | magic;         // bytes 0, 2 of w0
+    r[1] = ((w0 >> 8) & 0x00FF00FFu) | magic;  // bytes 1, 3 of w0
+    r[2] = (w1 & 0x00FF00FFu) | magic;         // bytes 0, 2 of w1
+    r[3] = ((w1 >> 8) & 0x00FF00FFu) | magic;  // bytes 1, 3 of w1
 }
 
 // 2-bit: the lane's 8 codes are the 16 bits at bit 16 * (t & 1) of word w.
@@ -256,8 +429,8 @@ __device__ __forceinline__ int odd_word(int t) { return (BITS * t) >> 2; }
 template <int BITS>
 __device__ __forceinline__ uint32_t odd_shift(int t) { return static_cast<uint32_t>(((BITS * t) & 3) * 8); }
 
-// Unpack lane t's 8 codes of the k32 block starting at `blk` (4-byte aligned,
-// 8-byte aligned for 8-bit codes). Used by the unpack diagnostic.
+// Unpack lane t's 8 codes of the k32 block starting at `blk` (4-byte aligned).
+// Used by the unpack diagnostic.
 template <int BITS>
 __device__ __forceinline__ void unpack_block(const uint32_t* blk, int t, uint32_t (&r)[4]) {
     if constexpr (BITS == 2) {
@@ -265,7 +438,7 @@ __device__ __forceinline__ void unpack_block(const uint32_t* blk, int t, uint32_
     } else if constexpr (BITS == 4) {
         unpack4(blk[t], r);
     } else if constexpr (BITS == 8) {
-        unpack8(blk[2 * t], blk[2 * t + 1], r);
+        unpack8(blk[t], blk[4 + t], r);
     } else {
         // a block holds BITS words; the next word is read only when it is still
         // inside the block (3-bit lane 3 fits in its first word)

@@ -1,0 +1,132 @@
+// Host-side helpers shared by qmm_api.cu and qmm_noalloc.cu (see qmm_host.h).
+#include "qmm_host.h"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace qmmk {
+
+int stages_for(int bits, int group, int mb, int optin) {
+    const int st = stage_count(bits, group, mb);
+    return (st >= 2 && main_smem_bytes(bits, group, mb) <= optin) ? st : 0;
+}
+
+int chunk_count(int64_t K, int group) { return static_cast<int>((K / group + kGPC - 1) / kGPC); }
+
+// Per-CTA cost model, fitted on GB300 to the 4-bit group-64 K=17408 N=5120
+// projection over 1, 2, 4 and 8 slices: a CTA pays, per row block of up to 128
+// rows, one pass over its slice's chunks (chunk bytes at about 28 GB/s per SM)
+// plus about 2 us of restart, and slicing adds about 3.7 us for the partial
+// sums and their reduce. The work is cut evenly over (bank, slice, row) space,
+// so when the CTA count is not a multiple of the bank-slice segments some CTA
+// ranges straddle two segments and pay one more row block. Slices keep at
+// least 2 chunks.
+int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, int num_sms, int cap) {
+    const int C = chunk_count(K, group);
+    const double chunk_us = kTN * (chunk_row_bytes(bits, group) + 4.0 * kGPC) / 28e3;
+    const double row_block_us = 2.0;
+    const double split_us = 3.7;
+    int best = 1;
+    double best_cost = 0.0;
+    for (int s = 1; s <= cap; ++s) {
+        if (s > 1 && C / s < 2) break;
+        const int64_t rows_total = banks * s * N;
+        int64_t ctas = (rows_total + kSlab - 1) / kSlab;
+        if (ctas > num_sms) ctas = num_sms;
+        const int64_t rows_per_cta = (rows_total + ctas - 1) / ctas;
+        int64_t blocks = (rows_per_cta + kTN - 1) / kTN;
+        if (ctas % (banks * s) != 0) ++blocks;
+        const int per_slice = (C + s - 1) / s;
+        const double cost = blocks * (per_slice * chunk_us + row_block_us) + (s > 1 ? split_us : 0.0);
+        if (s == 1 || cost < best_cost) {
+            best = s;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+cudaError_t configure_format(int bits, int group, int mb, int smem_bytes) {
+    switch (bits) {
+        case 2: return configure_kernels<2>(group, mb, smem_bytes);
+        case 3: return configure_kernels<3>(group, mb, smem_bytes);
+        case 4: return configure_kernels<4>(group, mb, smem_bytes);
+        case 5: return configure_kernels<5>(group, mb, smem_bytes);
+        case 6: return configure_kernels<6>(group, mb, smem_bytes);
+        case 8: return configure_kernels<8>(group, mb, smem_bytes);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_format(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,
+                          const MainParams<kMaxBanks>* banked, const MainParams<2>* fused) {
+    switch (bits) {
+        case 2: return launch_forward<2>(group, L, single, banked, fused);
+        case 3: return launch_forward<3>(group, L, single, banked, fused);
+        case 4: return launch_forward<4>(group, L, single, banked, fused);
+        case 5: return launch_forward<5>(group, L, single, banked, fused);
+        case 6: return launch_forward<6>(group, L, single, banked, fused);
+        case 8: return launch_forward<8>(group, L, single, banked, fused);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+namespace {
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+}  // namespace
+
+bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group, CUtensorMap* out) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const int W = wbox_width(bits, group);
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(K * bits / 8);
+    const cuuint64_t dims[2] = {row_bytes, static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(W), static_cast<cuuint32_t>(kTN)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = W == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                           : (W == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_sb_map(const void* a, int64_t G, int64_t N, CUtensorMap* out) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGPC), static_cast<cuuint32_t>(kTN)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_x_map(const void* x, int M, int64_t K, int group, int mb, CUtensorMap* out) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr || M < 1 || K % 64 != 0) return false;
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(chunk_codes(group) / 64), 8};   // one 8-row tile
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace qmmk

@@ -21,34 +21,21 @@ cudaError_t configure_one(int smem_bytes) {
 
 template <int BITS, int GROUP, int MB, int CAP>
 cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
-    // The main kernel is a programmatic dependent of the staging kernel: it is
-    // scheduled once every staging CTA has started and waits (griddepcontrol.wait)
-    // before touching what the staging kernel writes. For up to 8 rows the staging
-    // kernel is a programmatic dependent of what precedes it too, and so resident
-    // (waiting) before that work ends. For 9..16 rows it is an ordinary launch:
-    // launched early, its CTAs take the first SMs the previous main kernel frees,
-    // a few to an SM, and the next main kernel's CTAs on those SMs wait for them to
-    // exit; that costs more than the later start (22.9 against 24.4 us/call on a
-    // 5120 x 17408 projection, the same within 1% on the other shapes measured).
+    // The main kernel is a programmatic dependent of whatever precedes it on the
+    // stream: it is scheduled as soon as that work allows (its CTAs take SMs as
+    // the preceding grid's CTAs leave them) and streams weights at once; its
+    // staging warps wait (griddepcontrol.wait) for that work to finish before
+    // they read x.
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    // (1) activation staging
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(mp.h.C));
-    cfg.blockDim = dim3(kXprepThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.gridDim = dim3(static_cast<unsigned>(L.ctas));
+    cfg.blockDim = dim3(main_threads(MB));
+    cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
     cfg.stream = L.stream;
     cfg.attrs = attr;
-    cfg.numAttrs = MB == 16 ? 0 : 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, qmm_xprep_kernel<BITS, GROUP, MB>, L.x, L.M, mp.h.K, mp.h.G,
-                                       const_cast<uint8_t*>(mp.h.xprep));
-    if (e != cudaSuccess) return e;
     cfg.numAttrs = 1;
-    // (2) main kernel: loads weights at once, waits for (1) before its staged activations
-    cfg.gridDim = dim3(static_cast<unsigned>(L.ctas));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
     return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP>, mp);
 }
 

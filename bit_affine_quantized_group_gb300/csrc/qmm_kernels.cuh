@@ -1,24 +1,25 @@
 // qmm kernels for sm_103a.
 //
 // Per forward call, in stream order:
-//   1. qmm_xprep_kernel   -- stages x once per call: MMA B fragments in the
-//                            permuted k order the unpackers produce, the per-group
-//                            activation sums XS (the "b*XS" term of the
-//                            dequant-after-dot form, vmlx-swift PR #565, LaneQMM
-//                            commit) as split binary16 fragments, and one
-//                            power-of-two range factor per (row, chunk).
-//   2. qmm_main_kernel    -- one CTA per SM; a producer warp streams packed code
-//                            rows (TMA 2-D tensor boxes), scales and biases (TMA
-//                            boxes, or 4-byte cp.async pieces when a row of them
-//                            is not 16-byte aligned) and the staged activations
-//                            (one bulk copy per chunk) into a ring of shared-
-//                            memory stages; eight consumer warps unpack the
-//                            codes in registers and contract them on tensor cores,
+//   1. qmm_main_kernel    -- one CTA per SM, launched as a programmatic
+//                            dependent of the preceding work on the stream.
+//                            A producer warp streams packed code rows (TMA 2-D
+//                            tensor boxes), scales and biases (TMA boxes, or
+//                            4-byte cp.async pieces when a row of them is not
+//                            16-byte aligned) into a ring of shared-memory
+//                            stages from the moment the CTA starts and, once the
+//                            preceding work has finished, the chunk's raw
+//                            activation rows (bulk copies); staging warps turn
+//                            the raw activations into the chunk's tensor-core
+//                            fragments, the per-group activation sums XS (the
+//                            "b*XS" term of the dequant-after-dot form,
+//                            vmlx-swift PR #565, LaneQMM commit) and the range
+//                            factors; eight consumer warps unpack the codes in
+//                            registers and contract them on tensor cores,
 //                            reading each code byte once for all M rows (same
-//                            page, qwen_qmv_rows_full commit: weights read once per
-//                            k-block for all rows). Launched as a programmatic
-//                            dependent of (1): code loads start before (1) ends.
-//   3. qmm_splitk_reduce_kernel (splits > 1 only) -- sums the fp32 slice
+//                            page, qwen_qmv_rows_full commit: weights read once
+//                            per k-block for all rows).
+//   2. qmm_splitk_reduce_kernel (splits > 1 only) -- sums the fp32 slice
 //                            partials in slice order (same page, "JANGH split-K
 //                            verify tile" commit: FP32 partials, then a sum).
 //
@@ -33,7 +34,10 @@
 // which is  sum_g s*P + b*XS.  The s*P' part is one FMA per accumulator per
 // group (plus one per chunk for 1/f); the (b, s) x (XS, -XSc) part is a small
 // binary16 MMA per chunk, with XS and XSc split into high and low binary16
-// halves so each keeps ~22 bits.
+// halves so each keeps ~22 bits. The staging warps obtain f*XS and f*XSc/1024
+// from the staged fragments themselves with a tensor-core MMA against a
+// constant selector (column 2q sums group q with weights 2^j, column 2q + 1
+// with weights 1).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -43,6 +47,16 @@
 #include "qmm_device.cuh"
 
 namespace qmmk {
+
+// f(integral_constant<int, I>) for I = B .. E - 1, so that I is a compile-time
+// constant inside f (shared-memory offsets become load immediates).
+template <int B, int E, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    if constexpr (B < E) {
+        f(std::integral_constant<int, B>{});
+        static_for<B + 1, E>(f);
+    }
+}
 
 constexpr int kMaxBanks = 64;
 
@@ -56,27 +70,23 @@ struct BankPtrs {
 enum OutMode : int { kOutF32 = 0, kOutBF16 = 1, kOutPartial = 2 };
 
 // Kernel parameters. CAP = number of bank slots carried (1 for a single
-// projection, kMaxBanks for banked calls), so single calls pass a small block.
+// projection, kMaxBanks for banked calls, 2 for the fused gate/up projection),
+// so single calls pass a small block.
 struct MainHeader {
-    const uint8_t* xprep;   // per chunk: xprep_chunk_bytes(bits, group, MB)
+    const uint16_t* x;      // activations [M][K] bfloat16, 16-byte aligned
     float* partial;         // [banks][splits][M][N] when out_mode == kOutPartial
     uint32_t* err;          // device error word
     int64_t N;
     int64_t K;
-    int64_t row_bytes;      // K*bits/8
-    int64_t rows_total;     // banks * splits * N
-    int64_t xprep_bytes;    // extent of the staged-activation region (for copy checks)
+    int64_t rows_total;     // banks * splits * N (1 * splits * N for the fused projection)
     int G;                  // K / group
     int C;                  // chunks = ceil(G / 8)
     int splits;
     int M;
-    int stages;
     int out_mode;
     int sb_tma;             // scales/biases by TMA boxes (G % 8 == 0), else cp.async
-    int sb_vec16;           // scale/bias rows 16-byte aligned (G % 8 == 0)
     int banks;
-    int swiglu;             // fused gate/up (the two-bank kernel): out = silu(gate) * up
-    float* gate;            // [M][N] fp32 gate results of the current call (swiglu, unsliced)
+    float* gate;            // [M][N] fp32 gate results of the current call (fused gate/up, unsliced)
     uint32_t unpack_magic;  // kF16x2_1024, given at run time so it stays in a register
 };
 
@@ -87,6 +97,7 @@ struct MainParams {
     CUtensorMap tmw[CAP];   // packed codes: uint8 [N][row_bytes], box kTN x W, swizzled
     CUtensorMap tms[CAP];   // scales: uint16 [N][G], box kTN x 8 (when sb_tma)
     CUtensorMap tmb[CAP];   // biases: same
+    CUtensorMap tmx;        // activations: bf16 [M][K/64][64] (x rows in 64-code blocks), box 64 x CK/64 x 8
 };
 
 struct ReduceParams {
@@ -101,228 +112,95 @@ struct ReduceParams {
 };
 
 // ---------------------------------------------------------------------------
-// Work enumeration shared by the producer and the consumers: the flattened
-// (bank, split, row) space is cut evenly over the CTAs; a CTA's range is cut at
-// (bank, split) boundaries and then into balanced row blocks of <= kTN rows.
+// Work enumeration shared by every warp role. The flattened (bank, split, row)
+// space is cut evenly over the CTAs; a CTA's range is cut at (bank, split)
+// boundaries and then into balanced row blocks of <= kTN rows; every row block
+// walks the chunks of its K slice. One item = one chunk of one row block (for
+// the fused gate/up projection, each row block is walked for bank 0 (gate) and
+// then for bank 1 (up)).
 // ---------------------------------------------------------------------------
-template <bool SWIGLU, typename F>
-__device__ __forceinline__ void for_each_row_block(const MainHeader& p, F&& f) {
-    const int64_t r_begin = p.rows_total * blockIdx.x / gridDim.x;
-    const int64_t r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
-    int64_t r = r_begin;
-    while (r < r_end) {
-        const int64_t seg = r / p.N;                                  // bank * splits + split
-        const int64_t seg_end = min(r_end, (seg + 1) * p.N);
-        const int64_t len = seg_end - r;
-        const int nb = static_cast<int>((len + kTN - 1) / kTN);
-        // fused gate/up: the flattened space is (split, row) and every row block
-        // is run for bank 0 (gate) and then bank 1 (up) by the same CTA
-        const int bank = SWIGLU ? 0 : static_cast<int>(seg / p.splits);
-        const int split = static_cast<int>(seg % p.splits);
-        const int c0 = static_cast<int>(static_cast<int64_t>(split) * p.C / p.splits);
-        const int c1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.C / p.splits);
-        for (int ib = 0; ib < nb; ++ib) {
-            const int64_t a = r + len * ib / nb;
-            const int64_t e = r + len * (ib + 1) / nb;
-            if constexpr (SWIGLU) {
-                if (!f(0, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
-                if (!f(1, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
-            } else {
-                if (!f(bank, split, a - seg * p.N, static_cast<int>(e - a), c0, c1)) return;
-            }
+template <bool SWIGLU>
+struct WorkIter {
+    int64_t r, r_end;       // flattened rows of this CTA still to start, end
+    int64_t seg;            // bank * splits + split of the current segment
+    int64_t seg_end;
+    int64_t a0, len;        // first flattened row and length of the segment part
+    int nb, ib;             // row blocks of the part, current one
+    int pass;               // fused gate/up: 0 = gate, 1 = up
+    int bank, split, rows, c0, c1, c;
+    int64_t n0;             // first weight row of the current row block
+    bool valid;
+
+    __device__ __forceinline__ void init(const MainHeader& p) {
+        r = p.rows_total * blockIdx.x / gridDim.x;
+        r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
+        start_segment(p);
+    }
+    __device__ __forceinline__ void start_segment(const MainHeader& p) {
+        valid = r < r_end;
+        if (!valid) return;
+        seg = r / p.N;
+        seg_end = min(r_end, (seg + 1) * p.N);
+        a0 = r;
+        len = seg_end - r;
+        nb = static_cast<int>((len + kTN - 1) / kTN);
+        ib = 0;
+        pass = 0;
+        split = static_cast<int>(seg % p.splits);
+        c0 = static_cast<int>(static_cast<int64_t>(split) * p.C / p.splits);
+        c1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.C / p.splits);
+        start_block(p);
+    }
+    __device__ __forceinline__ void start_block(const MainHeader& p) {
+        const int64_t a = a0 + len * ib / nb;
+        const int64_t e = a0 + len * (ib + 1) / nb;
+        n0 = a - seg * p.N;
+        rows = static_cast<int>(e - a);
+        bank = SWIGLU ? pass : static_cast<int>(seg / p.splits);
+        c = c0;
+    }
+    __device__ __forceinline__ bool block_start() const { return c == c0; }
+    __device__ __forceinline__ bool block_end() const { return c == c1 - 1; }
+    __device__ __forceinline__ void next(const MainHeader& p) {
+        if (++c < c1) return;
+        if (SWIGLU && pass == 0) {
+            pass = 1;
+            bank = 1;
+            c = c0;
+            return;
+        }
+        pass = 0;
+        if (++ib < nb) {
+            start_block(p);
+            return;
         }
         r = seg_end;
+        start_segment(p);
     }
-}
+};
 
 // ---------------------------------------------------------------------------
-// 1. Activation staging.
+// Small helpers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
 }
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t v) { return __uint_as_float(v << 16); }
-
-// 16 bytes of x through L2 (x may have been written on other SMs just before).
-__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
-
-// One CTA per chunk, one warp per scale group of the chunk. For 8-row tile j,
-// lane (g, t) of warp gg holds activation row m = 8j + g and, of each k32 block
-// vb of the group, the 8-code piece 4vb + t (codes 32vb + 8t .. 32vb + 8t + 7),
-// so the four lanes of a quad hold the group's codes of one row:
-//   XS[m,g]  = sum_{k in g} x[m,k],   XSc[m,g] = sum_{k in g} x[m,k] * 1024 * 2^-j(k),
-// summed over each piece in code order, then over the lane's pieces and the
-// quad in a fixed tree order. f = 2^(14 - e) from the binary exponent e of the
-// chunk's largest |x| (clamped so f and 1/f stay normal), sigma = 2^(e' - 13)
-// from the largest |XS|, |XSc| of the chunk (exponent e'), both over the eight
-// groups through shared memory. Rows m >= M and codes past the end of K stage
-// as zeros (f = sigma = 1).
-template <int BITS, int GROUP, int MB>
-__global__ void __launch_bounds__(kXprepThreads)
-qmm_xprep_kernel(const uint16_t* __restrict__ x, int M, int64_t K, int G, uint8_t* __restrict__ xprep) {
-    static_assert(kXprepThreads == 32 * kGPC, "one warp per scale group");
-    constexpr int CK = kGPC * GROUP;                 // codes per chunk
-    constexpr int VPG = GROUP / 32;                  // k32 blocks per group
-    constexpr int NT = n8_tiles(MB);
-    constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
-    constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
-
-    // The main kernel may start loading weights while this runs. This kernel may
-    // itself be launched as a programmatic dependent of whatever ran before it on
-    // the stream, so it waits for that work (which may produce x, or still read
-    // the staging buffer) before touching x or the buffer.
-    griddep_launch_dependents();
-    griddep_wait();
-
-    __shared__ float s_xs[MB][kGPC];      // XS
-    __shared__ float s_xsc[MB][kGPC];     // XSc
-    __shared__ uint32_t s_mag[MB][kGPC];  // largest |x| bit pattern of the group
-
-    const int c = blockIdx.x;
-    const int gg = threadIdx.x >> 5;                 // this warp's group
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2;
-    const int t = lane & 3;
-    const int64_t k0 = static_cast<int64_t>(c) * CK;
-    const int kc = min(kGPC, G - c * kGPC) * GROUP;  // codes of this chunk inside K
-    const bool x16 = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-
-    // every load first
-    uint4 v[NT][VPG];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        const int m = 8 * j + g;
-        const uint16_t* row = x + static_cast<int64_t>(m) * K + k0;
-#pragma unroll
-        for (int u = 0; u < VPG; ++u) {
-            const int k = 32 * (gg * VPG + u) + 8 * t;
-            v[j][u] = make_uint4(0, 0, 0, 0);
-            if (m < M && k < kc) {
-                if (x16) {
-                    v[j][u] = ld_cg_v4(row + k);
-                } else {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = static_cast<uint32_t>(__ldcg(row + k + 2 * e)) |
-                               (static_cast<uint32_t>(__ldcg(row + k + 2 * e + 1)) << 16);
-                    v[j][u] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-    }
-    // group sums and magnitude of each row
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        float s = 0.0f, sc = 0.0f;
-        uint32_t mag = 0;
-#pragma unroll
-        for (int u = 0; u < VPG; ++u) {
-            const uint32_t wv[4] = {v[j][u].x, v[j][u].y, v[j][u].z, v[j][u].w};
-            float ps = 0.0f, psc = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uint32_t hbits = (wv[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
-                const float xv = bf16_bits_to_float(hbits);
-                ps += xv;
-                psc = fmaf(xv, 1024.0f / static_cast<float>(1 << code_shift(BITS, e)), psc);
-                mag = max(mag, hbits & 0x7FFFu);
-            }
-            s = u == 0 ? ps : s + ps;
-            sc = u == 0 ? psc : sc + psc;
-        }
-        s += __shfl_xor_sync(0xFFFFFFFFu, s, 1);
-        sc += __shfl_xor_sync(0xFFFFFFFFu, sc, 1);
-        s += __shfl_xor_sync(0xFFFFFFFFu, s, 2);
-        sc += __shfl_xor_sync(0xFFFFFFFFu, sc, 2);
-        mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));
-        mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 2));
-        if (t == 0) {
-            s_xs[8 * j + g][gg] = s;
-            s_xsc[8 * j + g][gg] = sc;
-            s_mag[8 * j + g][gg] = mag;
-        }
-    }
-    __syncthreads();
-
-    uint8_t* out = xprep + static_cast<size_t>(c) * XPB;
-    uint4* frag = reinterpret_cast<uint4*>(out);
-    uint4* bias = reinterpret_cast<uint4*>(out + XFB);
-    float* tail = reinterpret_cast<float*>(out + XFB + xprep_bias_bytes(MB));
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-        const int m = 8 * j + g;
-        float amax = 0.0f;
-        uint32_t mag = 0;
-#pragma unroll
-        for (int q = 0; q < kGPC; ++q) {
-            amax = fmaxf(amax, fmaxf(fabsf(s_xs[m][q]), fabsf(s_xsc[m][q])));
-            mag = max(mag, s_mag[m][q]);
-        }
-        // sigma puts the largest |XS/sigma|, |XSc/sigma| in [2^13, 2^14): inside the
-        // binary16 range with room to spare
-        float sg = 1.0f;
-        if (amax > 0.0f && amax <= 3.0e38f) sg = ldexpf(1.0f, ilogbf(amax) - 13);
-        const float rsig = 1.0f / sg;    // exact: power of two
-        // every f*x*2^-j is below 2^15, and any x within 2^27 of the largest is
-        // exact in binary16
-        int ex = 0;
-        if (mag != 0) ex = min(127, max(-100, static_cast<int>(mag >> 7) - 127));
-        const float f = (mag != 0) ? ldexpf(1.0f, 14 - ex) : 1.0f;
-        if (gg == 0 && t == 0) {
-            tail[m] = sg;
-            tail[MB + m] = 1.0f / f;   // exact: power of two
-        }
-        // MMA B fragments of this group's k32 blocks, in the unpackers' slot order
-#pragma unroll
-        for (int u = 0; u < VPG; ++u) {
-            const int vb = gg * VPG + u;
-            const uint32_t wv[4] = {v[j][u].x, v[j][u].y, v[j][u].z, v[j][u].w};
-            uint32_t r[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c0 = slot_code(BITS, q, 0), c1 = slot_code(BITS, q, 1);
-                const float lo = bf16_bits_to_float((wv[c0 >> 1] >> (16 * (c0 & 1))) & 0xFFFFu) * f *
-                                 (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 0)));
-                const float hi = bf16_bits_to_float((wv[c1 >> 1] >> (16 * (c1 & 1))) & 0xFFFFu) * f *
-                                 (1.0f / static_cast<float>(1 << slot_shift(BITS, q, 1)));
-                r[q] = pack_half2(__float2half_rn(lo), __float2half_rn(hi));
-            }
-            frag[(vb * NT + j) * 32 + lane] = make_uint4(r[0], r[1], r[2], r[3]);
-        }
-        // bias-term fragments of tile j (warp j): groups 2t and 2t + 1 of row m,
-        // XS and -XSc over sigma, each as a high and a low binary16 half
-        if (gg == j) {
-            const float v0 = s_xs[m][2 * t] * rsig;
-            const float v1 = s_xs[m][2 * t + 1] * rsig;
-            const float w0 = -s_xsc[m][2 * t] * rsig;
-            const float w1 = -s_xsc[m][2 * t + 1] * rsig;
-            const __half v0h = __float2half_rn(v0), v1h = __float2half_rn(v1);
-            const __half w0h = __float2half_rn(w0), w1h = __float2half_rn(w1);
-            const __half v0l = __float2half_rn(v0 - __half2float(v0h)), v1l = __float2half_rn(v1 - __half2float(v1h));
-            const __half w0l = __float2half_rn(w0 - __half2float(w0h)), w1l = __float2half_rn(w1 - __half2float(w1h));
-            bias[j * 32 + lane] =
-                make_uint4(pack_half2(v0h, v1h), pack_half2(w0h, w1h), pack_half2(v0l, v1l), pack_half2(w0l, w1l));
-        }
-    }
+// float from a power-of-two exponent (e in the normal range)
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float(static_cast<uint32_t>(e + 127) << 23); }
+// bfloat16 half h of a packed pair, as float
+__device__ __forceinline__ float bf16_half(uint32_t w, int h) {
+    return __uint_as_float(h ? (w & 0xFFFF0000u) : (w << 16));
 }
+constexpr uint32_t kF16One = 0x3C00u;
+QMM_HD constexpr uint32_t f16_pow2_bits(int e) { return static_cast<uint32_t>(e + 15) << 10; }   // 2^e, -14 <= e <= 15
 
-// ---------------------------------------------------------------------------
-// 2. Main kernel.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void consumer_barrier() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kNCW * 32) : "memory");
-}
-
-// Byte offset, inside a stage, of byte b of weight-tile row r (TMA box layout
-// with the W-byte swizzle: 16-byte chunk bits 4.. of the in-box address are
-// XORed with its bits 7..).
+// Byte offset, inside a stage's weight tile, of byte b of tile row r (TMA box
+// layout with the W-byte swizzle: bits 4.. of the in-box address are XORed
+// with its bits 7..).
 template <int BITS, int GROUP>
 __device__ __forceinline__ int wtile_off(int r, int b) {
     constexpr int W = wbox_width(BITS, GROUP);
@@ -332,52 +210,89 @@ __device__ __forceinline__ int wtile_off(int r, int b) {
     return ((b >> LW) << (LW + 7)) + (lin ^ (((lin >> 7) & MASK) << 4));
 }
 
+// ---------------------------------------------------------------------------
+// The main kernel.
+// ---------------------------------------------------------------------------
 template <int BITS, int GROUP, int MB, int CAP>
-__global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
-    constexpr int VB = vblocks_per_group(BITS, GROUP);
+__global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
     constexpr int NT = n8_tiles(MB);
+    constexpr int NSW = staging_warps(MB);
+    constexpr int NCW = consumer_warps(MB);
+    constexpr int CPAR = consumer_parities(MB);
+    constexpr int WPPC = NCW / CPAR;             // consumer warps of one parity
+    constexpr int VB = vblocks_per_group(GROUP);
+    constexpr int VPC = vblocks_per_chunk(GROUP);
+    constexpr int CK = chunk_codes(GROUP);
     constexpr int BB = vblock_bytes(BITS);
     constexpr int RB = chunk_row_bytes(BITS, GROUP);
     constexpr int W = wbox_width(BITS, GROUP);
     constexpr int NBOX = wbox_count(BITS, GROUP);
-    constexpr int SW = stage_weight_bytes(BITS, GROUP);
+    constexpr int SWB = stage_weight_bytes(BITS, GROUP);
     constexpr int SSB = stage_sb_bytes();
-    constexpr int XFB = xprep_frag_bytes(BITS, GROUP, MB);
-    constexpr int XPB = xprep_chunk_bytes(BITS, GROUP, MB);
-    constexpr int SB = stage_bytes(BITS, GROUP, MB);
-    constexpr int NV = kGroupsPerWarp * VB;        // k32 blocks per consumer warp per stage
-    const MainHeader& p = P.h;
-    // the two-bank parameter block is the fused gate/up projection's
+    constexpr int WSB = wstage_bytes(BITS, GROUP);          // weight stage
+    constexpr int ASB = aslot_bytes(GROUP, MB);             // activation slot
+    constexpr int XRB = xraw_bytes(GROUP, MB);
+    constexpr int NBX = CK / 64;                    // 64-code blocks per chunk
+    // weight stage: codes [NBOX][kTN][W] swizzled, then
+    constexpr int OFF_S = SWB;                      // scales [kTN][8] binary16
+    constexpr int OFF_B = OFF_S + SSB;              // biases [kTN][8] binary16
+    // activation slot:
+    constexpr int XRT = XRB / NT;                   // raw x of one 8-row tile
+    constexpr int OFF_XR = 0;                       // raw x [NT][8][NBX][128 B], 128-byte swizzle
+    constexpr int OFF_XF = XRB;                     // B fragments [VPC][NT][32] x 16 B
+    constexpr int OFF_XB = OFF_XF + xfrag_bytes(GROUP, MB);   // bias fragments [NT][32] x 16 B
+    constexpr int OFF_XT = OFF_XB + xbias_bytes(MB);          // sigma[MB], 1/f[MB]
     constexpr bool SWIGLU = CAP == 2;
+    static_assert(W * NBOX == RB, "weight boxes");
+    static_assert(XRT % 1024 == 0 && OFF_XT + 8 * MB <= ASB && OFF_B + SSB <= WSB, "stage layout");
+    const MainHeader& p = P.h;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
     // array so every access below stays a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int S = p.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
-    uint64_t* empty = full + S;
-    float* scratch = reinterpret_cast<float*>(smem + S * SB + S * 16);
+    constexpr int S = stage_count(BITS, GROUP, MB);     // weight stages
+    constexpr int F = act_slots(BITS, GROUP, MB);       // activation slots
+    static_assert(S >= 2 && F >= 2 && S % CPAR == 0 && F % CPAR == 0, "pipeline depth");
+    uint8_t* aring = smem + S * WSB;                                        // activation slots
+    uint64_t* wfull = reinterpret_cast<uint64_t*>(aring + F * ASB);        // weights, scales, biases landed
+    uint64_t* wempty = wfull + S;                                          // weight stage consumed
+    uint64_t* xfull = wempty + S;                                          // raw activations landed [F][NT]
+    uint64_t* sfull = xfull + F * NT;                                      // fragments staged
+    uint64_t* fempty = sfull + F;                                          // activation slot consumed
+    float* combine = reinterpret_cast<float*>(fempty + F);                 // [kSlabs][NT][4][32]
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1 + 32);      // producer lane 0 (expect_tx) + 32 cp.async arrivals
-            mbar_init(&empty[i], kNCW);
+            // producer lane 0 (expect_tx), plus 32 cp.async arrivals when the
+            // scales and biases come by cp.async
+            mbar_init(&wfull[i], p.sb_tma ? 1 : 1 + 32);
+            mbar_init(&wempty[i], WPPC);          // one lane of each of the stage parity's consumer warps
+        }
+        for (int i = 0; i < F * NT; ++i)
+            mbar_init(&xfull[i], 1);              // the owning staging warp's lane 0 (expect_tx), per tile
+        for (int i = 0; i < F; ++i) {
+            mbar_init(&sfull[i], NT);             // one lane of the owning staging warp of each tile
+            mbar_init(&fempty[i], WPPC);          // one lane of each of the slot parity's consumer warps
         }
         fence_barrier_init();
     }
     __syncthreads();
+    // The next kernel on the stream may be scheduled now; its CTAs take the SMs
+    // this grid's CTAs free and start streaming their own weights at once.
     griddep_launch_dependents();
 
-    if (warp == kNCW) {
+    if (warp == NCW + NSW) {
         // ------------------------------ producer ------------------------------
-        // Lane 0 issues the TMA boxes of a stage (packed codes, scales, biases)
-        // and the bulk copy of its staged activations. Scales and biases whose
-        // rows are not 16-byte multiples go through per-lane cp.async instead.
+        // Lane 0 issues the TMA boxes of a stage (packed codes, scales, biases).
+        // Scales and biases whose rows are not 16-byte multiples go through
+        // per-lane cp.async instead. The weights do not depend on the preceding
+        // work on the stream, so this warp never waits for it.
         const uint64_t pol = policy_evict_first();
-        if (lane == 0)
+        if (lane == 0) {
+            prefetch_tensormap(&P.tmx);
             for (int i = 0; i < p.banks && i < CAP; ++i) {
                 prefetch_tensormap(&P.tmw[i]);
                 if (p.sb_tma) {
@@ -385,378 +300,677 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_main_kernel(const __grid_cons
                     prefetch_tensormap(&P.tmb[i]);
                 }
             }
-        const uint32_t tx_stage =
-            static_cast<uint32_t>(NBOX * kTN * W + (p.sb_tma ? 2 * SSB : 0) + XPB);
+        }
+        const uint32_t tx_stage = static_cast<uint32_t>(NBOX * kTN * W + (p.sb_tma ? 2 * SSB : 0));
+        WorkIter<SWIGLU> wi;
+        wi.init(p);
         uint32_t it = 0;
-        int pslot = 0;            // it % S, kept incrementally (S is a run-time value)
-        uint32_t pround = 0;      // it / S
-        bool waited = false;
+        int slot = 0;             // it % S, kept incrementally
+        uint32_t round = 0;       // it / S
         bool ok = true;
-        int npend = 0;
-        int pend_slot[kMaxStages];
-        int pend_chunk[kMaxStages];
-        auto issue_xprep = [&](int slot, int c) {
-            uint8_t* d = smem + slot * SB + SW + 2 * SSB;
-            const int64_t off = static_cast<int64_t>(c) * XPB;
-            if (slot < 0 || slot >= S || c < 0 || off + XPB > p.xprep_bytes ||
-                ((reinterpret_cast<uintptr_t>(p.xprep + off) | smem_u32(d)) & 15)) {
-                record_bad_copy(p.err, p.xprep + off, static_cast<uint64_t>(slot) << 32 | static_cast<uint32_t>(c), 3u);
-                return;
+        bool sb_ok = true;
+        for (; wi.valid; wi.next(p)) {
+            const BankPtrs bp = P.bank[wi.bank];
+            if (wi.block_start()) {
+                // the cp.async path for scales/biases checks its buffers once per row block
+                sb_ok = p.sb_tma ||
+                    (wi.n0 >= 0 && wi.rows >= 1 && wi.rows <= kTN && wi.n0 + wi.rows <= p.N && wi.c0 >= 0 &&
+                     wi.c1 <= p.C && ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & 3) == 0);
+                if (!sb_ok && lane == 0) record_bad_copy(p.err, bp.s, static_cast<uint64_t>(wi.rows), 4u);
             }
-            bulk_g2s(d, p.xprep + off, XPB, &full[slot]);
-        };
-        auto flush_pending = [&]() {
-            griddep_wait();   // the staged activations of this call are ready
-            waited = true;
-            if (lane == 0)
-                for (int i = 0; i < npend; ++i) issue_xprep(pend_slot[i], pend_chunk[i]);
-            npend = 0;
-        };
-        for_each_row_block<SWIGLU>(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
-            (void)split;
-            const BankPtrs bp = P.bank[bank];
-            // the cp.async path for scales/biases checks its buffers once per row block
-            const bool sb_ok = p.sb_tma ||
-                (n0 >= 0 && rows >= 1 && rows <= kTN && n0 + rows <= p.N && c0 >= 0 && c1 <= p.C &&
-                 ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & 3) == 0);
-            if (!sb_ok && lane == 0) record_bad_copy(p.err, bp.s, static_cast<uint64_t>(rows), 4u);
-            for (int c = c0; c < c1; ++c) {
-                const int slot = pslot;
-                // After a timed-out wait the error is recorded and no further waits are
-                // made; the loop still runs to the end so that every warp finishes.
-                // (The slot's previous use was in round pround - 1: parity pround ^ 1.)
-                if (it >= static_cast<uint32_t>(S) && ok &&
-                    !mbar_wait(&empty[slot], (pround ^ 1u) & 1u, p.err, kErrEmptyWait))
-                    ok = false;
-                uint8_t* st = smem + slot * SB;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&full[slot], tx_stage);
-                    const int y = static_cast<int>(n0);
+            // After a timed-out wait the error is recorded and no further waits are
+            // made; the loop still runs to the end so that every warp finishes.
+            // (The slot's previous use was in round `round - 1`: parity round ^ 1.)
+            if (it >= static_cast<uint32_t>(S) && ok &&
+                !mbar_wait_sleep(&wempty[slot], (round ^ 1u) & 1u, p.err, kErrEmptyWait, 128u))
+                ok = false;
+            uint8_t* st = smem + slot * WSB;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&wfull[slot], tx_stage);
+                const int y = static_cast<int>(wi.n0);
 #pragma unroll
-                    for (int bi = 0; bi < NBOX; ++bi)
-                        tma_load_2d(st + bi * (kTN * W), &P.tmw[bank], c * RB + bi * W, y, &full[slot], pol);
-                    if (p.sb_tma) {
-                        tma_load_2d(st + SW, &P.tms[bank], c * kGPC, y, &full[slot], pol);
-                        tma_load_2d(st + SW + SSB, &P.tmb[bank], c * kGPC, y, &full[slot], pol);
-                    }
-                }
-                __syncwarp();
-                if (!p.sb_tma && sb_ok) {
-                    const int ng = min(kGPC, p.G - c * kGPC);
-                    const int nq = ng >> 1;   // 4-byte pieces per row
-                    uint8_t* sdst = st + SW;
-                    uint8_t* bdst = sdst + SSB;
-                    const uint16_t* ssrc = bp.s + n0 * p.G + c * kGPC;
-                    const uint16_t* bsrc = bp.b + n0 * p.G + c * kGPC;
-                    for (int i = lane; i < rows * nq; i += 32) {
-                        const int r = i / nq, q = i - (i / nq) * nq;
-                        cp_async_4(sdst + r * 16 + 4 * q, ssrc + static_cast<int64_t>(r) * p.G + 2 * q);
-                        cp_async_4(bdst + r * 16 + 4 * q, bsrc + static_cast<int64_t>(r) * p.G + 2 * q);
-                    }
-                }
-                cp_async_arrive_noinc(&full[slot]);
-                if (waited) {
-                    if (lane == 0) issue_xprep(slot, c);
-                } else {
-                    pend_slot[npend] = slot;
-                    pend_chunk[npend] = c;
-                    if (++npend == S) flush_pending();
-                }
-                ++it;
-                if (++pslot == S) {
-                    pslot = 0;
-                    ++pround;
+                for (int bi = 0; bi < NBOX; ++bi)
+                    tma_load_2d(st + bi * (kTN * W), &P.tmw[wi.bank], wi.c * RB + bi * W, y, &wfull[slot], pol);
+                if (p.sb_tma) {
+                    tma_load_2d(st + OFF_S, &P.tms[wi.bank], wi.c * kGPC, y, &wfull[slot], pol);
+                    tma_load_2d(st + OFF_B, &P.tmb[wi.bank], wi.c * kGPC, y, &wfull[slot], pol);
                 }
             }
-            return true;
-        });
-        if (!waited) flush_pending();
+            __syncwarp();
+            if (!p.sb_tma && sb_ok) {
+                const int ng = min(kGPC, p.G - wi.c * kGPC);
+                const int nq = ng >> 1;   // 4-byte pieces per row
+                uint8_t* sdst = st + OFF_S;
+                uint8_t* bdst = st + OFF_B;
+                const uint16_t* ssrc = bp.s + wi.n0 * p.G + wi.c * kGPC;
+                const uint16_t* bsrc = bp.b + wi.n0 * p.G + wi.c * kGPC;
+                for (int i = lane; i < wi.rows * nq; i += 32) {
+                    const int rr = i / nq, q = i - (i / nq) * nq;
+                    cp_async_4(sdst + rr * 16 + 4 * q, ssrc + static_cast<int64_t>(rr) * p.G + 2 * q);
+                    cp_async_4(bdst + rr * 16 + 4 * q, bsrc + static_cast<int64_t>(rr) * p.G + 2 * q);
+                }
+            }
+            if (!p.sb_tma) cp_async_arrive_noinc(&wfull[slot]);
+            ++it;
+            if (++slot == S) {
+                slot = 0;
+                ++round;
+            }
+        }
         // This warp's own cp.async copies must land before it exits.
         cp_async_wait_all();
         if (!ok) {
             // Give the copies already issued a bounded chance to land before exiting.
             const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0u;
             for (uint32_t i = first; i < it; ++i)
-                if (!mbar_wait(&full[i % S], (i / S) & 1u, p.err, kErrDrainWait)) break;
+                if (!mbar_drain(&wfull[i % S], (i / S) & 1u, p.err)) break;
         }
         return;
     }
 
-    // -------------------------------- consumers --------------------------------
-    const uint32_t magic = p.unpack_magic;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const uint32_t sel2 = unpack2_selector(t);   // 2-bit codes only
-    const int sp = warp % kSlabPairs;        // slabs sp and sp + 4
-    const int kh = warp / kSlabPairs;        // chunk groups 4*kh .. 4*kh + 3
-    const int gbase = kh * kGroupsPerWarp;
-    const int vbw = gbase * VB;              // first k32 block of this warp in a chunk
-    // Offsets of this lane's codes in each of the warp's k32 blocks, for a tile
-    // row r with r % 8 == 0 (add r * W): box base + swizzled 16-byte chunk +
-    // byte. 4-bit: one word (block = one 16-byte chunk); 8-bit: two words
-    // (block = two chunks). Both use 128-byte boxes.
-    int cx[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const int vb = vbw + i;
-        if constexpr (BITS == 4)
-            cx[i] = ((vb >> 3) << 14) + ((((vb & 7) ^ g) << 4) | (4 * t));
-        else if constexpr (BITS == 8)
-            cx[i] = ((vb >> 2) << 14) + (((((2 * vb + (t >> 1)) & 7) ^ g) << 4) | (8 * (t & 1)));
-        else
-            cx[i] = 0;
-    }
-    int cslot = 0;            // stage index % S, kept incrementally
-    uint32_t cphase = 0;      // (stage index / S) & 1
-    bool ok = true;
-    for_each_row_block<SWIGLU>(p, [&](int bank, int split, int64_t n0, int rows, int c0, int c1) -> bool {
-        const int nsl = (rows + kSlab - 1) / kSlab;
-        bool act[kSPW];
-        int row0[kSPW];
-#pragma unroll
-        for (int sw = 0; sw < kSPW; ++sw) {
-            const int slab = sp + sw * kSlabPairs;
-            act[sw] = slab < nsl;
-            row0[sw] = slab * kSlab + g;
-        }
-        float acc[kSPW][NT][4];
-#pragma unroll
-        for (int sw = 0; sw < kSPW; ++sw)
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[sw][j][e] = 0.0f;
 
-        for (int c = c0; c < c1; ++c) {
-            const int slot = cslot;
-            // a timed-out wait is recorded; the warp then stops waiting but keeps the
-            // same control flow, so the consumer barriers below are always reached
-            if (ok && !mbar_wait(&full[slot], cphase, p.err, kErrFullWait)) ok = false;
-            const int ng = min(kGPC, p.G - c * kGPC);
-            const uint8_t* st = smem + slot * SB;
-            const uint8_t* wst = st;
-            const uint16_t* sst = reinterpret_cast<const uint16_t*>(st + SW);
-            const uint16_t* bst = reinterpret_cast<const uint16_t*>(st + SW + SSB);
-            const uint4* xfr = reinterpret_cast<const uint4*>(st + SW + 2 * SSB);
-            const uint4* xbias = reinterpret_cast<const uint4*>(st + SW + 2 * SSB + XFB);
-            const float* xsig = reinterpret_cast<const float*>(st + SW + 2 * SSB + XFB + xprep_bias_bytes(MB));
-            const float* xrf = xsig + MB;            // 1/f per activation row
-
-            // this warp's 4 scales for each of its slab rows (binary16 pairs)
-            uint2 sv0[kSPW], sv1[kSPW];
+    if (warp >= NCW) {
+        // ------------------------------ staging -------------------------------
+        // Warp (j, par) stages activation tile j (rows 8j .. 8j + 7) of the
+        // stages in its slots, the whole chunk: lane (g, t) handles row
+        // m = 8j + g and, in each k32 block, the 8 codes it holds in the
+        // consumers' fragments. Everything it needs across lanes (the row's
+        // largest |x| and the bias-term range) reduces inside the quad.
+        constexpr int SPT = staging_per_tile(MB);
+        const int sw = warp - NCW;
+        const int j = sw / SPT;
+        const int par = sw % SPT;
+        const int m = 8 * j + g;
+        // Selector of the XS MMA: column n = g of B belongs to group q = g >> 1
+        // of a half chunk, XS (even n, weight 2^j per k slot) or XSc/1024 (odd
+        // n, weight 1). k slots 2t + e and 2t + 8 + e of MMA u are the slots
+        // (r = 2u, e) and (r = 2u + 1, e) of the unpackers. selq[q] is the
+        // selector for group q of the half (zero in the other groups' columns).
+        uint32_t selq[4][2][2];
 #pragma unroll
-            for (int sw = 0; sw < kSPW; ++sw) {
-                sv0[sw] = *reinterpret_cast<const uint2*>(sst + row0[sw] * 8 + gbase);
-                sv1[sw] = *reinterpret_cast<const uint2*>(sst + (row0[sw] + 8) * 8 + gbase);
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int rr = 2 * u + kk;
+                    const uint32_t xs =
+                        f16_pow2_bits(slot_shift(BITS, rr, 0)) | (f16_pow2_bits(slot_shift(BITS, rr, 1)) << 16);
+                    selq[q][u][kk] = (g >> 1) != q ? 0u : ((g & 1) ? (kF16One | (kF16One << 16)) : xs);
+                }
+        constexpr int HPC = VPC / 2;                  // k32 blocks per half chunk (groups 0-3 / 4-7)
+        // with groups of 32 the raw values of a chunk stay in registers between
+        // the two passes; with groups of 64 they are read from shared memory twice
+        constexpr bool KEEP = VPC <= 8;
+
+        // Warp par of the tile owns the activation slots f with f % SPT == par:
+        // it issues its tile's raw-activation copies (one 3-D TMA box of x per
+        // chunk: the tile's 8 rows, refilled with the chunk F items ahead as soon
+        // as the staging has read it) and writes its tile's fragments. Every phase of a slot's barriers is
+        // therefore awaited, in order, by the one warp that owns the slot (a
+        // parity wait may only run one phase ahead of its barrier). x is read
+        // only after the preceding work on the stream (which may have produced
+        // it) has finished.
+        auto issue_raw = [&](int f, int c) {
+            uint64_t* bar = &xfull[f * NT + j];
+            if (c < 0 || c >= p.C) {
+                record_bad_copy(p.err, p.x, static_cast<uint64_t>(f) << 32 | static_cast<uint32_t>(c), 5u);
+                mbar_arrive(bar);   // complete the phase without data
+                return;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(XRT));
+            tma_load_3d(aring + f * ASB + OFF_XR + j * XRT, &P.tmx, 0, c * NBX, 8 * j, bar);
+        };
+        griddep_wait();
+        // The items of this warp's slots are the items it with it % STRIDE == par;
+        // it walks them only (warps with par >= STRIDE own no slot).
+        constexpr int STRIDE = F <= SPT ? F : SPT;
+        static_assert(F <= SPT || F % SPT == 0, "activation slot ownership");
+        if (par >= STRIDE) return;
+        WorkIter<SWIGLU> lead;   // the item F ahead of the current one
+        lead.init(p);
+        uint32_t issued = 0;     // one past the last item whose raw copy this warp issued
+        for (int i = 0; i < F && lead.valid; ++i, lead.next(p))
+            if (i % STRIDE == par) {
+                if (lane == 0) issue_raw(i, lead.c);
+                issued = static_cast<uint32_t>(i) + 1u;
             }
 
-            // The group loop, instantiated twice: without any guard for the common
-            // case (full chunk, both slabs live) so loads of later groups can be
-            // scheduled under the tensor-core work of earlier ones, and guarded for
-            // partial chunks and partial row blocks.
-            // Per-chunk sums sum_g s*P' (still scaled by f), folded into acc with 1/f.
-            float accc[kSPW][NT][4];
-            auto groups = [&](auto full_tag) {
-                constexpr bool FULL = decltype(full_tag)::value;
-                if constexpr (!FULL) {
-#pragma unroll
-                    for (int sw = 0; sw < kSPW; ++sw)
-#pragma unroll
-                        for (int j = 0; j < NT; ++j)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) accc[sw][j][e] = 0.0f;
-                }
-#pragma unroll
-                for (int gl = 0; gl < kGroupsPerWarp; ++gl) {
-                    if (!FULL && gbase + gl >= ng) continue;
-                    float P[kSPW][NT][4];
-#pragma unroll
-                    for (int v = 0; v < VB; ++v) {
-                        const int vi = gl * VB + v;          // block index within the warp
-                        const int vb = vbw + vi;             // block index within the chunk
-                        uint4 bf[NT];
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) bf[j] = xfr[(vb * NT + j) * 32 + lane];
-#pragma unroll
-                        for (int sw = 0; sw < kSPW; ++sw) {
-                            if (!FULL && !act[sw]) continue;
-                            uint32_t ra[4], rb[4];
-                            if constexpr (BITS == 4) {
-                                const uint8_t* a0 = wst + (row0[sw] - g) * W + cx[vi];
-                                unpack4(*reinterpret_cast<const uint32_t*>(a0 + g * W), ra, magic);
-                                unpack4(*reinterpret_cast<const uint32_t*>(a0 + (g + 8) * W), rb, magic);
-                            } else if constexpr (BITS == 8) {
-                                const uint8_t* a0 = wst + (row0[sw] - g) * W + cx[vi];
-                                const uint2 u0 = *reinterpret_cast<const uint2*>(a0 + g * W);
-                                const uint2 u1 = *reinterpret_cast<const uint2*>(a0 + (g + 8) * W);
-                                unpack8(u0.x, u0.y, ra, magic);
-                                unpack8(u1.x, u1.y, rb, magic);
-                            } else if constexpr (BITS == 2) {
-                                // lane t's 8 codes are half of word t / 2 of the block
-                                const int b0 = vb * BB + 4 * odd_word<BITS>(t);
-                                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(row0[sw], b0));
-                                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(row0[sw] + 8, b0));
-                                unpack2(w0, sel2, ra, magic);
-                                unpack2(w1, sel2, rb, magic);
-                            } else {
-                                const int b0 = vb * BB + 4 * odd_word<BITS>(t);
-                                const int r0 = row0[sw], r1 = row0[sw] + 8;
-                                const uint32_t lo0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r0, b0));
-                                const uint32_t hi0 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r0, b0 + 4));
-                                const uint32_t lo1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r1, b0));
-                                const uint32_t hi1 = *reinterpret_cast<const uint32_t*>(wst + wtile_off<BITS, GROUP>(r1, b0 + 4));
-                                unpack_odd<BITS>(lo0, hi0, odd_shift<BITS>(t), ra, magic);
-                                unpack_odd<BITS>(lo1, hi1, odd_shift<BITS>(t), rb, magic);
-                            }
-#pragma unroll
-                            for (int j = 0; j < NT; ++j) {
-                                if (v == 0)
-                                    mma_f16_zc(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
-                                else
-                                    mma_f16(P[sw][j], ra[0], rb[0], ra[1], rb[1], bf[j].x, bf[j].y);
-                                mma_f16(P[sw][j], ra[2], rb[2], ra[3], rb[3], bf[j].z, bf[j].w);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int sw = 0; sw < kSPW; ++sw) {
-                        if (!FULL && !act[sw]) continue;
-                        const uint32_t w0 = (gl < 2) ? sv0[sw].x : sv0[sw].y;
-                        const uint32_t w1 = (gl < 2) ? sv1[sw].x : sv1[sw].y;
-                        const float s0 = __half2float(__ushort_as_half(static_cast<uint16_t>(w0 >> (16 * (gl & 1)))));
-                        const float s1 = __half2float(__ushort_as_half(static_cast<uint16_t>(w1 >> (16 * (gl & 1)))));
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            if (FULL && gl == 0) {
-                                accc[sw][j][0] = s0 * P[sw][j][0];
-                                accc[sw][j][1] = s0 * P[sw][j][1];
-                                accc[sw][j][2] = s1 * P[sw][j][2];
-                                accc[sw][j][3] = s1 * P[sw][j][3];
-                            } else {
-                                accc[sw][j][0] = fmaf(s0, P[sw][j][0], accc[sw][j][0]);
-                                accc[sw][j][1] = fmaf(s0, P[sw][j][1], accc[sw][j][1]);
-                                accc[sw][j][2] = fmaf(s1, P[sw][j][2], accc[sw][j][2]);
-                                accc[sw][j][3] = fmaf(s1, P[sw][j][3], accc[sw][j][3]);
-                            }
-                        }
-                    }
+        // After a timed-out wait no further copies are issued; the ones in
+        // flight (this warp's items failed .. issued - 1) are drained before the
+        // warp exits.
+        bool ok = true;
+        uint32_t failed = 0;
+        WorkIter<SWIGLU> wi;
+        wi.init(p);
+#pragma unroll 1
+        for (int k = 0; k < par; ++k) {
+            wi.next(p);
+            lead.next(p);
+        }
+        uint32_t it = static_cast<uint32_t>(par);
+        for (; wi.valid; it += STRIDE) {
+            const int slot = static_cast<int>(it % static_cast<uint32_t>(F));
+            const uint32_t phase = (it / static_cast<uint32_t>(F)) & 1u;
+            if (ok && !mbar_wait(&xfull[slot * NT + j], phase, p.err, kErrFullWait)) {
+                ok = false;
+                failed = it;
+            }
+            uint8_t* st = aring + slot * ASB;
+            // refill the slot with the raw activations of the item F ahead
+            auto refill = [&]() {
+                __syncwarp();
+                if (ok && lead.valid) {
+                    if (lane == 0) issue_raw(slot, lead.c);
+                    issued = it + static_cast<uint32_t>(F) + 1u;
                 }
             };
-            if (ng == kGPC && act[0] && act[1])
-                groups(std::true_type{});
-            else
-                groups(std::false_type{});
+            // Tile row g, 64-code block b: 128 bytes at u = g * NBX + b (times 128)
+            // of the tile's raw area, with 16-byte piece c stored at piece c ^ (u & 7).
+            // Rows >= M and codes past K arrive from the TMA as zeros.
+            auto load_raw = [&](int vb, uint32_t (&v)[4]) {
+                const int u = g * NBX + (vb >> 1);
+                const uint8_t* rb = st + OFF_XR + j * XRT + u * 128;
+                const int key = u & 7;
+                if constexpr (BITS == 8) {
+                    // codes 4t .. 4t + 3 and 16 + 4t .. 16 + 4t + 3 of the k32 block
+                    const int c0 = (vb & 1) * 4 + (t >> 1), c1 = c0 + 2;
+                    const uint2 a0 = *reinterpret_cast<const uint2*>(rb + ((c0 ^ key) << 4) + (t & 1) * 8);
+                    const uint2 a1 = *reinterpret_cast<const uint2*>(rb + ((c1 ^ key) << 4) + (t & 1) * 8);
+                    v[0] = a0.x;
+                    v[1] = a0.y;
+                    v[2] = a1.x;
+                    v[3] = a1.y;
+                } else {
+                    // codes 8t .. 8t + 7 of the k32 block
+                    const uint4 a = *reinterpret_cast<const uint4*>(rb + ((((vb & 1) * 4 + t) ^ key) << 4));
+                    v[0] = a.x;
+                    v[1] = a.y;
+                    v[2] = a.z;
+                    v[3] = a.w;
+                }
+            };
+            uint32_t keep[KEEP ? VPC : 1][4];
+            // pass 1: largest |x| of row m over the chunk (the lane's codes as a
+            // tree, then the quad)
+            uint32_t bm[VPC];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const float2 rf = *reinterpret_cast<const float2*>(xrf + 8 * j + 2 * t);
+            for (int vb = 0; vb < VPC; ++vb) {
+                uint32_t v[4];
+                load_raw(vb, v);
+                bm[vb] = bf16x2_absmax(bf16x2_absmax(v[0], v[1]), bf16x2_absmax(v[2], v[3]));
+                if constexpr (KEEP) {
 #pragma unroll
-                for (int sw = 0; sw < kSPW; ++sw) {
-                    if (!act[sw]) continue;
-                    acc[sw][j][0] = fmaf(rf.x, accc[sw][j][0], acc[sw][j][0]);
-                    acc[sw][j][1] = fmaf(rf.y, accc[sw][j][1], acc[sw][j][1]);
-                    acc[sw][j][2] = fmaf(rf.x, accc[sw][j][2], acc[sw][j][2]);
-                    acc[sw][j][3] = fmaf(rf.y, accc[sw][j][3], acc[sw][j][3]);
+                    for (int e = 0; e < 4; ++e) keep[vb][e] = v[e];
                 }
             }
+#pragma unroll
+            for (int w2 = VPC / 2; w2 >= 1; w2 /= 2)
+#pragma unroll
+                for (int i = 0; i < w2; ++i) bm[i] = bf16x2_absmax(bm[i], bm[i + w2]);
+            if constexpr (KEEP) refill();
+            // the fragment area must be free: the consumers are done with the item F before
+            if (it >= static_cast<uint32_t>(F))
+                mbar_wait_sleep(&fempty[slot], phase ^ 1u, p.err, kErrEmptyWait, 128u);
+            const uint32_t mx = bm[0];
+            uint32_t mag = max(mx & 0x7FFFu, (mx >> 16) & 0x7FFFu);
+            mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 1));
+            mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, 2));
+            // f puts the chunk's largest |x| of the row in [2^14, 2^15): every
+            // f*x*2^-j is below 2^15, and any x within 2^27 of the largest is exact
+            int ex = 0;
+            if (mag != 0) ex = min(127, max(-100, static_cast<int>(mag >> 7) - 127));
+            const float f = pow2f(14 - ex);
+            const float rf = pow2f(ex - 14);
+            float fs[4][2];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) fs[rr][e] = f * pow2f(-slot_shift(BITS, rr, e));
 
-            // bias and offset terms of the chunk, (b | s) x (XS | -XSc) / sigma:
-            // K half kh takes slab kh of its pair
+            // pass 2: fragments, and f*XS, f*XSc/1024 per group through the selector MMA
+            // (accumulator 2h + (vb & 1): half h of the chunk, even/odd blocks)
+            float D[4][4];
 #pragma unroll
-            for (int sw = 0; sw < kSPW; ++sw) {
-                if (sw != kh || !act[sw]) continue;
-                uint32_t a0 = *reinterpret_cast<const uint32_t*>(bst + row0[sw] * 8 + 2 * t);
-                uint32_t a1 = *reinterpret_cast<const uint32_t*>(bst + (row0[sw] + 8) * 8 + 2 * t);
-                uint32_t a2 = *reinterpret_cast<const uint32_t*>(sst + row0[sw] * 8 + 2 * t);
-                uint32_t a3 = *reinterpret_cast<const uint32_t*>(sst + (row0[sw] + 8) * 8 + 2 * t);
-                if (ng < kGPC) {
-                    // groups past the end of K: stale shared memory, zero it
-                    const uint32_t keep = (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
-                    a0 &= keep;
-                    a1 &= keep;
-                    a2 &= keep;
-                    a3 &= keep;
+            for (int a = 0; a < 4; ++a) D[a][0] = D[a][1] = D[a][2] = D[a][3] = 0.0f;
+#pragma unroll
+            for (int vb = 0; vb < VPC; ++vb) {
+                uint32_t v[4];
+                if constexpr (KEEP) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = keep[vb][e];
+                } else {
+                    load_raw(vb, v);
                 }
+                uint32_t fr[4];
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint4 bb = xbias[j * 32 + lane];
-                    float D[4];
-                    mma_f16_zc(D, a0, a1, a2, a3, bb.x, bb.y);
-                    mma_f16(D, a0, a1, a2, a3, bb.z, bb.w);
-                    const float2 sg = *reinterpret_cast<const float2*>(xsig + 8 * j + 2 * t);
-                    acc[sw][j][0] = fmaf(sg.x, D[0], acc[sw][j][0]);
-                    acc[sw][j][1] = fmaf(sg.y, D[1], acc[sw][j][1]);
-                    acc[sw][j][2] = fmaf(sg.x, D[2], acc[sw][j][2]);
-                    acc[sw][j][3] = fmaf(sg.y, D[3], acc[sw][j][3]);
+                for (int rr = 0; rr < 4; ++rr) {
+                    float v2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        int wi4, hf;
+                        if constexpr (BITS == 8) {
+                            // piece rr >> 1, word e, half rr & 1
+                            wi4 = 2 * (rr >> 1) + e;
+                            hf = rr & 1;
+                        } else {
+                            const int cc = slot_code(BITS, rr, e);
+                            wi4 = cc >> 1;
+                            hf = cc & 1;
+                        }
+                        v2[e] = bf16_half(v[wi4], hf) * fs[rr][e];
+                    }
+                    fr[rr] = f2_to_h2(v2[0], v2[1]);
+                }
+                *reinterpret_cast<uint4*>(st + OFF_XF + ((vb * NT + j) * 32 + lane) * 16) =
+                    make_uint4(fr[0], fr[1], fr[2], fr[3]);
+                const int hv = vb / HPC;                      // half chunk
+                const int q = (vb % HPC) / VB;                // group within the half
+                float (&Da)[4] = D[2 * hv + (vb & 1)];
+                mma_f16(Da, fr[0], 0u, fr[1], 0u, selq[q][0][0], selq[q][0][1]);
+                mma_f16(Da, fr[2], 0u, fr[3], 0u, selq[q][1][0], selq[q][1][1]);
+            }
+            if constexpr (!KEEP) refill();
+            // lane (g, t): groups t (half 0) and 4 + t (half 1) of row m
+            const float xs0 = (D[0][0] + D[1][0]) * rf, xsc0 = (D[0][1] + D[1][1]) * (rf * 1024.0f);
+            const float xs1 = (D[2][0] + D[3][0]) * rf, xsc1 = (D[2][1] + D[3][1]) * (rf * 1024.0f);
+            float am = fmaxf(fmaxf(fabsf(xs0), fabsf(xsc0)), fmaxf(fabsf(xs1), fabsf(xsc1)));
+            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+            am = fmaxf(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+            // sigma puts the largest |XS/sigma|, |XSc/sigma| of the row in [2^13, 2^14)
+            int es = 13;
+            if (am > 0.0f && am <= 3.0e38f) es = max(-100, static_cast<int>((__float_as_uint(am) >> 23) & 0xFFu) - 127);
+            const float rsig = pow2f(13 - es);    // 1 / sigma
+            const float sg = pow2f(es - 13);
+            uint32_t hi[2], lo[2];
+            {
+                const float vv[2] = {xs0 * rsig, xs1 * rsig};
+                const float ww[2] = {-xsc0 * rsig, -xsc1 * rsig};
+#pragma unroll
+                for (int hv = 0; hv < 2; ++hv) {
+                    const __half vh = __float2half_rn(vv[hv]), wh = __float2half_rn(ww[hv]);
+                    const __half vl = __float2half_rn(vv[hv] - __half2float(vh));
+                    const __half wl = __float2half_rn(ww[hv] - __half2float(wh));
+                    hi[hv] = pack_half2(vh, wh);
+                    lo[hv] = pack_half2(vl, wl);
                 }
             }
+#pragma unroll
+            for (int hv = 0; hv < 2; ++hv) {
+                const uint32_t hi_p = __shfl_xor_sync(0xFFFFFFFFu, hi[hv], 1);
+                const uint32_t lo_p = __shfl_xor_sync(0xFFFFFFFFu, lo[hv], 1);
+                if ((t & 1) == 0) {
+                    // groups 4hv + t and 4hv + t + 1 form the bias fragment of lane (g, 2hv + t / 2)
+                    const uint4 frag = make_uint4((hi[hv] & 0xFFFFu) | (hi_p << 16), (hi[hv] >> 16) | (hi_p & 0xFFFF0000u),
+                                                  (lo[hv] & 0xFFFFu) | (lo_p << 16), (lo[hv] >> 16) | (lo_p & 0xFFFF0000u));
+                    *reinterpret_cast<uint4*>(st + OFF_XB + (j * 32 + g * 4 + 2 * hv + (t >> 1)) * 16) = frag;
+                }
+            }
+            if (t == 0) {
+                float* xt = reinterpret_cast<float*>(st + OFF_XT);
+                xt[m] = sg;
+                xt[MB + m] = rf;
+            }
+            // the warp's fragment stores, ordered by the warp barrier before one lane's release
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            if (++cslot == S) {
-                cslot = 0;
-                cphase ^= 1u;
+            if (lane == 0) mbar_arrive(&sfull[slot]);
+#pragma unroll 1
+            for (int k = 0; k < STRIDE; ++k) {
+                wi.next(p);
+                lead.next(p);
             }
         }
-
-        // combine the two K halves in a fixed order: (first half) + (second half)
-        float* sc = scratch + ((sp * kSPW) * NT * 4) * 32;
-        if (kh == 1) {
-#pragma unroll
-            for (int sw = 0; sw < kSPW; ++sw)
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) sc[((sw * NT + j) * 4 + e) * 32 + lane] = acc[sw][j][e];
+        if (!ok && lane == 0) {
+            for (uint32_t i = failed; i < issued; i += STRIDE) {
+                const int f = static_cast<int>(i % static_cast<uint32_t>(F));
+                if (!mbar_drain(&xfull[f * NT + j], (i / static_cast<uint32_t>(F)) & 1u, p.err)) break;
+            }
         }
-        consumer_barrier();
-        if (kh == 0) {
-            const BankPtrs bp = P.bank[bank];
+        __syncwarp();
+        return;
+    }
+
+    // -------------------------------- consumers --------------------------------
+    // Warp (w, cp) owns the SPW 16-row slabs SPW*w .. SPW*w + SPW - 1 of every
+    // row block (slab z: tile rows 16z + g and 16z + g + 8), every group of the
+    // chunks in the stage slots of parity cp (all slots when CPAR == 1). The
+    // slabs of a warp share its activation fragment loads and give it SPW
+    // independent MMA chains.
+    constexpr int SPW = consumer_slabs(MB);
+    constexpr int WPP = kSlabs / SPW;            // consumer warps per parity
+    const int w = warp % WPP;
+    const int cp = warp / WPP;
+    const int r0 = kSlab * SPW * w + g;          // first slab's row; slab s: r0 + 16 s
+    const uint32_t magic = p.unpack_magic;
+    const uint32_t sel2 = unpack2_selector(t);   // 2-bit codes only
+    const uint32_t ring = smem_u32(smem);
+    // Per-lane code addresses of the first slab inside a stage (4- and 8-bit:
+    // ldmatrix row addresses; 2-bit: 16-byte chunks of row r0; 3/5/6-bit: the
+    // two words of each block of row r0). Row r0 + 8 has the same swizzle,
+    // 8 * W further; the slab s rows, 16 * s * W further.
+    constexpr int NOFF = BITS == 4 ? (VPC / 2 < 4 ? VPC / 2 : 4)
+                       : BITS == 8 ? 4
+                       : BITS == 2 ? RB / 16
+                       : 2 * VPC;
+    int off[NOFF];
+    {
+        const int lr = kSlab * SPW * w + ((lane >> 3) & 1) * 8 + (lane & 7);   // ldmatrix row of this lane
 #pragma unroll
-            for (int sw = 0; sw < kSPW; ++sw) {
-                if (!act[sw]) continue;
+        for (int i = 0; i < NOFF; ++i) {
+            if constexpr (BITS == 4) {
+                const int b = 2 * i + (lane >> 4);                       // k32 block = 16-byte chunk
+                off[i] = lr * 128 + (((b & 7) ^ (lane & 7)) << 4);
+            } else if constexpr (BITS == 8) {
+                const int k = 2 * i + (lane >> 4);                       // 16-byte chunk (half block)
+                off[i] = lr * 128 + (((k & 7) ^ (lane & 7)) << 4);
+            } else if constexpr (BITS == 2) {
+                off[i] = wtile_off<BITS, GROUP>(r0, 16 * i);
+            } else {
+                const int vb = i >> 1;
+                const int b = vb * BB + 4 * ((BITS * t) >> 2) + 4 * (i & 1);
+                // 3-bit lane 3 needs no second word: read its first word again
+                const int bb = (BITS == 3 && t == 3 && (i & 1)) ? b - 4 : b;
+                off[i] = wtile_off<BITS, GROUP>(r0, bb);
+            }
+        }
+    }
+    const uint32_t oddsh = static_cast<uint32_t>(((BITS * t) & 3) * 8);
+
+    int cslot = 0;            // item % S (weight stage), kept incrementally
+    uint32_t cphase = 0;      // (item / S) & 1
+    int aslot = 0;            // item % F (activation slot)
+    uint32_t aphase = 0;      // (item / F) & 1
+    // Each output sums its block's items in two halves, the items of even and of
+    // odd index (the two consumer parities when there are two; otherwise one
+    // warp keeps both sums), added at the end of the block: so row m of an
+    // output is bitwise the same whether the 8- or the 16-row kernel made it.
+    constexpr int NACC = CPAR == 1 ? 2 : 1;
+    float acc[NACC][SPW][NT][4];
+    uint32_t ipar = 0;        // item & 1
+    WorkIter<SWIGLU> wi;
+    wi.init(p);
+    for (; wi.valid; wi.next(p), ipar ^= 1u) {
+        if (wi.block_start()) {
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
+            for (int a = 0; a < NACC; ++a)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int nl = row0[sw] + 8 * h;
-                        if (nl >= rows) continue;
-                        const int64_t n = n0 + nl;
+                for (int sl = 0; sl < SPW; ++sl)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int m = 8 * j + 2 * t + e;
-                            if (m >= p.M) continue;
-                            float v = acc[sw][j][2 * h + e] + sc[((sw * NT + j) * 4 + 2 * h + e) * 32 + lane];
-                            if (p.out_mode == kOutPartial) {
-                                p.partial[((static_cast<int64_t>(bank) * p.splits + split) * p.M + m) * p.N + n] = v;
+                    for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[a][sl][jj][e] = 0.0f;
+        }
+        // (a warp whose first slab holds rows of the block computes all of its
+        // slabs; rows past the block are not stored)
+        const bool active = w * SPW * kSlab < wi.rows;
+        const int slot = cslot;
+        const int fslot = aslot;
+        // (S and F are multiples of CPAR, so both slots have the item's parity)
+        const bool mine = CPAR == 1 || slot % CPAR == cp;
+        // a timed-out wait is recorded; the warp then stops waiting but keeps the
+        // same control flow
+        if (mine) {
+        mbar_wait(&wfull[slot], cphase, p.err, kErrFullWait);
+        mbar_wait(&sfull[fslot], aphase, p.err, kErrFullWait);
+        if (active) {
+            const uint32_t st = ring + static_cast<uint32_t>(slot * WSB);
+            const uint32_t at = ring + static_cast<uint32_t>(S * WSB + fslot * ASB);
+            const uint32_t b_r0 = st + static_cast<uint32_t>(r0 * 16);   // rows r0 (+128: r0 + 8) of scales, biases
+            const uint32_t b_l = at + static_cast<uint32_t>(lane * 16);  // this lane's fragment vectors
+            const uint32_t b_t = at + static_cast<uint32_t>(t * 8);      // activation rows 2t, 2t + 1 of the factors
+            const int ng = min(kGPC, p.G - wi.c * kGPC);
+            // this lane's scales of rows r0 + 16 s and r0 + 16 s + 8 (8 binary16 values each)
+            uint32_t s0w[SPW][4], s1w[SPW][4];
+            static_for<0, SPW>([&](auto s_c) {
+                constexpr int sl = decltype(s_c)::value;
+                const uint4 sv0 = lds128_at<OFF_S + 256 * sl>(b_r0);
+                const uint4 sv1 = lds128_at<OFF_S + 256 * sl + 128>(b_r0);
+                s0w[sl][0] = sv0.x; s0w[sl][1] = sv0.y; s0w[sl][2] = sv0.z; s0w[sl][3] = sv0.w;
+                s1w[sl][0] = sv1.x; s1w[sl][1] = sv1.y; s1w[sl][2] = sv1.z; s1w[sl][3] = sv1.w;
+            });
+            if (ng < kGPC) {
+                // groups past the end of K (stale shared memory on the cp.async path):
+                // zero their scales so they contribute nothing
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t keep = (2 * i + 1 < ng) ? 0xFFFFFFFFu : (2 * i < ng ? 0x0000FFFFu : 0u);
+#pragma unroll
+                    for (int sl = 0; sl < SPW; ++sl) {
+                        s0w[sl][i] &= keep;
+                        s1w[sl][i] &= keep;
+                    }
+                }
+            }
+            // code addresses of this chunk (4/8-bit: ldmatrix rows; 2-bit: row r0's 16-byte chunks)
+            uint32_t cb[(BITS == 4 || BITS == 8 || BITS == 2) ? NOFF : 1];
+            if constexpr (BITS == 4 || BITS == 8 || BITS == 2) {
+#pragma unroll
+                for (int i = 0; i < NOFF; ++i) cb[i] = st + static_cast<uint32_t>(off[i]);
+            }
+            float accc[SPW][NT][4];
+            uint32_t q4[SPW][4];     // 4-bit: ldmatrix words of the current pair of blocks
+            uint4 q2a[SPW], q2b[SPW];   // 2-bit: the 16-byte chunk (two blocks) of rows r0, r0 + 8
+            static_for<0, kGPC>([&](auto gq_c) {
+                constexpr int gq = decltype(gq_c)::value;
+                // the group's products, by k16 half of the blocks: two independent
+                // MMA chains a slab, added when the group is done
+                float Pg[SPW][NT][2][4];
+                static_for<0, VB>([&](auto v_c) {
+                    constexpr int v = decltype(v_c)::value;
+                    constexpr int vb = gq * VB + v;              // k32 block within the chunk
+                    uint4 bf[NT];
+                    static_for<0, NT>([&](auto j_c) {
+                        constexpr int jj = decltype(j_c)::value;
+                        bf[jj] = lds128_at<OFF_XF + (vb * NT + jj) * 512>(b_l);
+                    });
+                    static_for<0, SPW>([&](auto s_c) {
+                        constexpr int sl = decltype(s_c)::value;
+                        constexpr int SO = sl * kSlab * W;       // slab offset inside a weight box
+                        uint32_t ra[4], rb[4];
+                        if constexpr (BITS == 4) {
+                            // one ldmatrix per pair of blocks (rows r0 and r0 + 8 of both)
+                            if constexpr ((vb & 1) == 0)
+                                ldmatrix_x4_at<(vb >> 3) * (kTN * 128) + SO>(cb[(vb >> 1) & 3], q4[sl][0], q4[sl][1],
+                                                                             q4[sl][2], q4[sl][3]);
+                            unpack4((vb & 1) ? q4[sl][2] : q4[sl][0], ra, magic);
+                            unpack4((vb & 1) ? q4[sl][3] : q4[sl][1], rb, magic);
+                        } else if constexpr (BITS == 8) {
+                            uint32_t d0, d1, d2, d3;
+                            ldmatrix_x4_at<(vb >> 2) * (kTN * 128) + SO>(cb[vb & 3], d0, d1, d2, d3);
+                            unpack8(d0, d2, ra, magic);
+                            unpack8(d1, d3, rb, magic);
+                        } else if constexpr (BITS == 2) {
+                            if constexpr ((vb & 1) == 0) {
+                                q2a[sl] = lds128_at<SO>(cb[vb >> 1]);
+                                q2b[sl] = lds128_at<SO + 8 * W>(cb[vb >> 1]);
+                            }
+                            const uint32_t wa = (vb & 1) ? ((t >> 1) ? q2a[sl].w : q2a[sl].z)
+                                                         : ((t >> 1) ? q2a[sl].y : q2a[sl].x);
+                            const uint32_t wb = (vb & 1) ? ((t >> 1) ? q2b[sl].w : q2b[sl].z)
+                                                         : ((t >> 1) ? q2b[sl].y : q2b[sl].x);
+                            unpack2(wa, sel2, ra, magic);
+                            unpack2(wb, sel2, rb, magic);
+                        } else {
+                            const uint32_t lo = st + static_cast<uint32_t>(off[2 * vb]);
+                            const uint32_t hi = st + static_cast<uint32_t>(off[2 * vb + 1]);
+                            const uint32_t lo0 = lds32_at<SO>(lo);
+                            const uint32_t hi0 = lds32_at<SO>(hi);
+                            const uint32_t lo1 = lds32_at<SO + 8 * W>(lo);
+                            const uint32_t hi1 = lds32_at<SO + 8 * W>(hi);
+                            unpack_odd<BITS>(lo0, hi0, oddsh, ra, magic);
+                            unpack_odd<BITS>(lo1, hi1, oddsh, rb, magic);
+                        }
+                        static_for<0, NT>([&](auto j_c) {
+                            constexpr int jj = decltype(j_c)::value;
+                            if constexpr (v == 0) {
+                                mma_f16_zc(Pg[sl][jj][0], ra[0], rb[0], ra[1], rb[1], bf[jj].x, bf[jj].y);
+                                mma_f16_zc(Pg[sl][jj][1], ra[2], rb[2], ra[3], rb[3], bf[jj].z, bf[jj].w);
+                            } else {
+                                mma_f16(Pg[sl][jj][0], ra[0], rb[0], ra[1], rb[1], bf[jj].x, bf[jj].y);
+                                mma_f16(Pg[sl][jj][1], ra[2], rb[2], ra[3], rb[3], bf[jj].z, bf[jj].w);
+                            }
+                        });
+                    });
+                });
+#pragma unroll
+                for (int sl = 0; sl < SPW; ++sl) {
+                    const float sa =
+                        __half2float(__ushort_as_half(static_cast<uint16_t>(s0w[sl][gq >> 1] >> (16 * (gq & 1)))));
+                    const float sb =
+                        __half2float(__ushort_as_half(static_cast<uint16_t>(s1w[sl][gq >> 1] >> (16 * (gq & 1)))));
+#pragma unroll
+                    for (int jj = 0; jj < NT; ++jj) {
+                        // (elements 0, 1: row r0; 2, 3: row r0 + 8; paired by row)
+                        float pg[4];
+                        add_x2(pg[0], pg[1], Pg[sl][jj][0][0], Pg[sl][jj][0][1], Pg[sl][jj][1][0], Pg[sl][jj][1][1]);
+                        add_x2(pg[2], pg[3], Pg[sl][jj][0][2], Pg[sl][jj][0][3], Pg[sl][jj][1][2], Pg[sl][jj][1][3]);
+                        if constexpr (gq == 0) {
+                            mul_x2(accc[sl][jj][0], accc[sl][jj][1], sa, sa, pg[0], pg[1]);
+                            mul_x2(accc[sl][jj][2], accc[sl][jj][3], sb, sb, pg[2], pg[3]);
+                        } else {
+                            fma_x2(accc[sl][jj][0], accc[sl][jj][1], sa, sa, pg[0], pg[1], accc[sl][jj][0],
+                                   accc[sl][jj][1]);
+                            fma_x2(accc[sl][jj][2], accc[sl][jj][3], sb, sb, pg[2], pg[3], accc[sl][jj][2],
+                                   accc[sl][jj][3]);
+                        }
+                    }
+                }
+            });
+            // bias and offset terms of the chunk, (b | s) x (XS | -XSc) / sigma
+            const uint32_t b_r0t = b_r0 + static_cast<uint32_t>(4 * t);
+            const uint32_t keep = ng >= kGPC ? 0xFFFFFFFFu
+                                : (2 * t + 1 < ng) ? 0xFFFFFFFFu : (2 * t < ng ? 0x0000FFFFu : 0u);
+            static_for<0, SPW>([&](auto s_c) {
+                constexpr int sl = decltype(s_c)::value;
+                // (groups past the end of K, stale shared memory on the cp.async path: zeroed)
+                const uint32_t a0 = lds32_at<OFF_B + 256 * sl>(b_r0t) & keep;
+                const uint32_t a1 = lds32_at<OFF_B + 256 * sl + 128>(b_r0t) & keep;
+                const uint32_t a2 = lds32_at<OFF_S + 256 * sl>(b_r0t) & keep;
+                const uint32_t a3 = lds32_at<OFF_S + 256 * sl + 128>(b_r0t) & keep;
+                static_for<0, NT>([&](auto j_c) {
+                    constexpr int jj = decltype(j_c)::value;
+                    const uint2 rfv = lds64_at<OFF_XT + 4 * (MB + 8 * jj)>(b_t);
+                    const uint2 sgv = lds64_at<OFF_XT + 4 * (8 * jj)>(b_t);
+                    const uint4 bb = lds128_at<OFF_XB + jj * 512>(b_l);
+                    const float2 rf = make_float2(__uint_as_float(rfv.x), __uint_as_float(rfv.y));
+                    const float2 sg = make_float2(__uint_as_float(sgv.x), __uint_as_float(sgv.y));
+                    float Dd[4];
+                    mma_f16_zc(Dd, a0, a1, a2, a3, bb.x, bb.y);
+                    mma_f16(Dd, a0, a1, a2, a3, bb.z, bb.w);
+                    // A = rf * accc + (sg * Dd + A), by pairs (columns 2t, 2t + 1)
+                    auto add = [&](float (&A)[SPW][NT][4]) {
+#pragma unroll
+                        for (int h = 0; h < 4; h += 2) {
+                            float u0, u1;
+                            fma_x2(u0, u1, sg.x, sg.y, Dd[h], Dd[h + 1], A[sl][jj][h], A[sl][jj][h + 1]);
+                            fma_x2(A[sl][jj][h], A[sl][jj][h + 1], rf.x, rf.y, accc[sl][jj][h], accc[sl][jj][h + 1],
+                                   u0, u1);
+                        }
+                    };
+                    if (NACC == 1 || ipar == 0)
+                        add(acc[0]);
+                    else
+                        add(acc[NACC - 1]);
+                });
+            });
+        }
+        // every value the warp read from the stage and the slot is in its
+        // registers and used; after the warp barrier one lane releases both
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&wempty[slot]);
+            mbar_arrive(&fempty[fslot]);
+        }
+        }
+        if (++cslot == S) {
+            cslot = 0;
+            cphase ^= 1u;
+        }
+        if (++aslot == F) {
+            aslot = 0;
+            aphase ^= 1u;
+        }
+
+        if (!wi.block_end()) continue;
+        if constexpr (NACC == 2) {
+            // even items + odd items
+#pragma unroll
+            for (int sl = 0; sl < SPW; ++sl)
+#pragma unroll
+                for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[0][sl][jj][e] += acc[1][sl][jj][e];
+        }
+        if constexpr (CPAR > 1) {
+            // add the second parity's partial sums in a fixed order: parity 0 + parity 1
+            float* sc = combine + (w * SPW * NT * 4) * 32 + lane;
+            if (cp == 1 && active) {
+#pragma unroll
+                for (int sl = 0; sl < SPW; ++sl)
+#pragma unroll
+                    for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sc[((sl * NT + jj) * 4 + e) * 32] = acc[0][sl][jj][e];
+            }
+            named_barrier(1, NCW * 32);
+            if (cp == 0 && active) {
+#pragma unroll
+                for (int sl = 0; sl < SPW; ++sl)
+#pragma unroll
+                    for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[0][sl][jj][e] += sc[((sl * NT + jj) * 4 + e) * 32];
+            }
+        }
+        if (cp == 0 && active) {
+            const BankPtrs bp = P.bank[wi.bank];
+#pragma unroll
+            for (int sl = 0; sl < SPW; ++sl) {
+#pragma unroll
+            for (int jj = 0; jj < NT; ++jj) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int nl = r0 + kSlab * sl + 8 * hh;
+                    if (nl >= wi.rows) continue;
+                    const int64_t n = wi.n0 + nl;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int mm = 8 * jj + 2 * t + e;
+                        if (mm >= p.M) continue;
+                        float v = acc[0][sl][jj][2 * hh + e];
+                        if (p.out_mode == kOutPartial) {
+                            p.partial[((static_cast<int64_t>(wi.bank) * p.splits + wi.split) * p.M + mm) * p.N + n] = v;
+                            continue;
+                        }
+                        if constexpr (SWIGLU) {
+                            // gate pass: keep the fp32 gate; up pass: the same thread
+                            // wrote this (m, n) gate in the gate pass of this row block
+                            if (wi.bank == 0) {
+                                p.gate[mm * p.N + n] = v;
                                 continue;
                             }
-                            if constexpr (SWIGLU) {
-                                // gate pass: keep the fp32 gate; up pass: the same thread
-                                // wrote this (m, n) gate in the gate pass of this row block
-                                if (bank == 0) {
-                                    p.gate[m * p.N + n] = v;
-                                    continue;
-                                }
-                                const float gv = p.gate[m * p.N + n];
-                                v = gv / (1.0f + expf(-gv)) * v;
-                            }
-                            if (p.out_mode == kOutF32) {
-                                static_cast<float*>(bp.out)[m * p.N + n] = v;
-                            } else {
-                                static_cast<__nv_bfloat16*>(bp.out)[m * p.N + n] = __float2bfloat16_rn(v);
-                            }
+                            const float gv = p.gate[mm * p.N + n];
+                            v = gv / (1.0f + expf(-gv)) * v;
+                        }
+                        if (p.out_mode == kOutF32) {
+                            static_cast<float*>(bp.out)[mm * p.N + n] = v;
+                        } else {
+                            static_cast<__nv_bfloat16*>(bp.out)[mm * p.N + n] = __float2bfloat16_rn(v);
                         }
                     }
                 }
             }
+            }
         }
-        consumer_barrier();   // the scratch is free again
-        return true;
-    });
-    (void)ok;
+        if constexpr (CPAR > 1) named_barrier(1, NCW * 32);   // the combine scratch is free again
+    }
 }
 
 // ---------------------------------------------------------------------------
-// 3. Split-K reduce: out = sum_{s=0..S-1} partial[s] in slice order.
+// 2. Split-K reduce: out = sum_{s=0..S-1} partial[s] in slice order.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kReduceThreads) qmm_splitk_reduce_kernel(const __grid_constant__ ReduceParams p);
 
@@ -781,7 +995,7 @@ __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restr
         const uint32_t* blk = reinterpret_cast<const uint32_t*>(reinterpret_cast<const uint8_t*>(w) + n * row_bytes + vb * BB);
         uint32_t r[4];
         unpack_block<BITS>(blk, t, r);
-        uint8_t* out = codes + n * K + vb * 32 + 8 * t;
+        uint8_t* out = codes + n * K + vb * 32;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -790,7 +1004,7 @@ __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restr
                 const int j = slot_shift(BITS, q, h);
                 const uint32_t mant = v & 0x3FFu;
                 const bool okv = (v & 0xFC00u) == 0x6400u && (mant & ((1u << j) - 1u)) == 0 && (mant >> j) < (1u << BITS);
-                out[slot_code(BITS, q, h)] = okv ? static_cast<uint8_t>(mant >> j) : static_cast<uint8_t>(0xFF);
+                out[block_code(BITS, t, q, h)] = okv ? static_cast<uint8_t>(mant >> j) : static_cast<uint8_t>(0xFF);
             }
         }
     }
@@ -800,8 +1014,6 @@ __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restr
 // Host-side launch helpers (defined per code width in qmm_inst_b*.cu).
 // ---------------------------------------------------------------------------
 struct LaunchCfg {
-    const uint16_t* x;
-    int M;
     int mb;            // 8 or 16
     int ctas;
     int smem;

@@ -2,17 +2,20 @@
 // device code (both sides of the library; nothing here is used by the oracle).
 //
 // Work decomposition (one main-kernel CTA per SM):
-//   * K is cut into chunks of kGPC = 8 scale groups; one pipeline stage holds
-//     one chunk for a row block of up to kTN = 128 weight rows: the packed
-//     code bytes of those rows (TMA tensor boxes), their 8 scales and 8 biases
-//     (TMA boxes), and the staged activation fragments of the chunk (one bulk
-//     copy).
-//   * A row block is 8 slabs of 16 rows. There are 8 consumer warps and one
-//     producer warp. Consumer warp w owns slabs (w % 4) and (w % 4) + 4 and
-//     the groups 4*(w / 4) .. 4*(w / 4) + 3 of every chunk, so each slab pair
-//     is split between two warps along K; their partial sums are added in a
-//     fixed order through a small shared-memory scratch at the end of the row
-//     block.
+//   * K is cut into chunks of kGPC = 8 scale groups. A CTA walks its rows in
+//     row blocks of up to kTN = 128 weight rows; one pipeline stage holds one
+//     chunk of one row block: the packed code bytes of those rows (TMA tensor
+//     boxes) and their 8 scales and 8 biases (TMA boxes). A separate ring of
+//     activation slots holds, per work item, the raw bfloat16 activation rows
+//     of the chunk (one TMA box per 8-row tile) and the chunk's staged
+//     activation fragments.
+//   * Warp roles: consumer_warps(MB) consumer warps (warp (w, p) owns
+//     consumer_slabs(MB) 16-row slabs of every row block, all 8 groups of
+//     every chunk, in the stage slots of parity p when there are two consumer
+//     parities; the two parities' partial sums are added at the end of the row
+//     block), staging_warps(MB) activation-staging warps (warp (j, p) turns the
+//     raw activations of 8-row tile j into tensor-core fragments in the
+//     activation slots it owns) and one weight-copy-issuing producer warp.
 //   * Inside a slab the contraction runs on tensor cores with
 //     mma.m16n8k16: A = 16 weight rows x 16 codes (unpacked to the exact
 //     binary16 values 1024 + q * 2^j), B = 16 codes x 8 activation rows (x
@@ -33,23 +36,37 @@ namespace qmmk {
 constexpr int kGPC = 8;            // scale groups per chunk (pipeline stage)
 constexpr int kTN = 128;           // weight rows per row block
 constexpr int kSlab = 16;          // rows per MMA slab
-constexpr int kSlabPairs = 4;      // consumer warps along the rows
-constexpr int kKParts = 2;         // consumer warps along K (halves of a chunk)
-constexpr int kNCW = kSlabPairs * kKParts;   // consumer warps
-constexpr int kSPW = 2;            // slabs per consumer warp
-constexpr int kGroupsPerWarp = kGPC / kKParts;
-constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kSlabs = kTN / kSlab; // 16-row slabs per row block
 constexpr int kMaxStages = 8;
-constexpr int kXprepThreads = 256;
+// Dynamic shared memory a CTA may opt into on sm_100-class GPUs (GB300: 227 KB).
+constexpr int kSmemOptin = 232448;
 constexpr int kReduceThreads = 256;
 
 QMM_HD constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
+QMM_HD constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 
-// k32 blocks per scale group.
-QMM_HD constexpr int vblocks_per_group(int bits, int group) { return (void)bits, group / 32; }
-QMM_HD constexpr int vblocks_per_chunk(int bits, int group) {
-    return kGPC * vblocks_per_group(bits, group);
-}
+// 8-row activation tiles of an MB-row kernel (MB = 8 or 16).
+QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
+// Staging warps: staging_per_tile(mb) per 8-row activation tile, warp p of a
+// tile owning the activation slots s with s % staging_per_tile == p.
+QMM_HD constexpr int staging_per_tile(int mb) { return mb == 8 ? 6 : 2; }
+QMM_HD constexpr int staging_warps(int mb) { return staging_per_tile(mb) * n8_tiles(mb); }
+// Consumer warps: consumer_slabs(mb) 16-row slabs per warp, one warp per slab
+// group and consumer parity. The 8-row kernel gives a warp two slabs (two
+// independent MMA chains sharing the activation fragment loads) and runs two
+// parities; the 16-row kernel's wider fragments need the registers of one slab
+// and one parity. Either way 8 consumer warps; with the staging warps and the
+// producer at most four warps share a scheduler, so 128 registers a thread.
+QMM_HD constexpr int consumer_slabs(int mb) { return mb == 8 ? 2 : 1; }
+QMM_HD constexpr int consumer_parities(int mb) { return mb == 8 ? 2 : 1; }
+QMM_HD constexpr int consumer_warps(int mb) { return kSlabs / consumer_slabs(mb) * consumer_parities(mb); }
+QMM_HD constexpr int main_threads(int mb) { return (consumer_warps(mb) + staging_warps(mb) + 1) * 32; }
+
+// k32 blocks per scale group and per chunk.
+QMM_HD constexpr int vblocks_per_group(int group) { return group / 32; }
+QMM_HD constexpr int vblocks_per_chunk(int group) { return kGPC * vblocks_per_group(group); }
+// Codes of one row in a full chunk.
+QMM_HD constexpr int chunk_codes(int group) { return kGPC * group; }
 // Bytes of one weight row that one k32 block consumes.
 QMM_HD constexpr int vblock_bytes(int bits) { return 4 * bits; }
 // Packed bytes of one weight row in a full chunk.
@@ -62,34 +79,78 @@ QMM_HD constexpr int wbox_width(int bits, int group) {
     return chunk_row_bytes(bits, group) % 128 == 0 ? 128 : (chunk_row_bytes(bits, group) % 64 == 0 ? 64 : 32);
 }
 QMM_HD constexpr int wbox_count(int bits, int group) { return chunk_row_bytes(bits, group) / wbox_width(bits, group); }
-QMM_HD constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 
-// Staged activations, per chunk: MMA B fragments (one 16-byte vector per lane
-// per k32 block per 8-row tile), the bias-term fragments, and two factors per
-// activation row (the bias-term range factor and 1/f, f the x range factor).
-QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
-QMM_HD constexpr int xprep_frag_bytes(int bits, int group, int mb) {
-    return vblocks_per_chunk(bits, group) * n8_tiles(mb) * 512;
-}
-QMM_HD constexpr int xprep_bias_bytes(int mb) { return n8_tiles(mb) * 512; }
-QMM_HD constexpr int xprep_chunk_bytes(int bits, int group, int mb) {
-    return round_up(xprep_frag_bytes(bits, group, mb) + xprep_bias_bytes(mb) + 2 * mb * 4, 128);
+// Staged activations of a chunk, written by the staging warps into the stage:
+// MMA B fragments (one 16-byte vector per lane per k32 block per 8-row tile),
+// the bias-term fragments (one 16-byte vector per lane per tile), and two
+// factors per activation row (the bias-term range factor sigma and 1/f, f the
+// x range factor).
+QMM_HD constexpr int xfrag_bytes(int group, int mb) { return vblocks_per_chunk(group) * n8_tiles(mb) * 512; }
+QMM_HD constexpr int xbias_bytes(int mb) { return n8_tiles(mb) * 512; }
+QMM_HD constexpr int xstaged_bytes(int group, int mb) {
+    return round_up(xfrag_bytes(group, mb) + xbias_bytes(mb) + 2 * mb * 4, 128);
 }
 
-// One pipeline stage in shared memory (1024-byte aligned: the swizzle atom).
+// Raw activations of one chunk, per 8-row tile one 3-D TMA box of x viewed as
+// [M rows][K/64 blocks][64 codes]: [MB/8][8][chunk_codes/64][128 bytes], each
+// 128-byte line stored with the 128-byte swizzle (so the staging warps' 16-byte
+// reads of 8 different rows fall in different banks); rows >= M arrive as zeros.
+QMM_HD constexpr int xraw_bytes(int group, int mb) { return 2 * chunk_codes(group) * mb; }
+
+// Weight stage (one chunk of one row block; 1024-byte aligned, the swizzle
+// atom): packed codes, scales, biases.
 QMM_HD constexpr int stage_weight_bytes(int bits, int group) { return kTN * chunk_row_bytes(bits, group); }
 QMM_HD constexpr int stage_sb_bytes() { return kTN * 16; }   // 8 binary16 values per row
-QMM_HD constexpr int stage_bytes(int bits, int group, int mb) {
-    return round_up(stage_weight_bytes(bits, group) + 2 * stage_sb_bytes() + xprep_chunk_bytes(bits, group, mb), 1024);
+QMM_HD constexpr int wstage_bytes(int bits, int group) {
+    return round_up(stage_weight_bytes(bits, group) + 2 * stage_sb_bytes(), 1024);
+}
+// Activation slot (one chunk): raw activations (1024-byte aligned) and the
+// staged fragments.
+QMM_HD constexpr int aslot_bytes(int group, int mb) { return round_up(xraw_bytes(group, mb) + xstaged_bytes(group, mb), 1024); }
+
+// Scratch for adding the second consumer parity's partial sums at the end of
+// a row block: [slab][tile][4][32 lanes] floats.
+QMM_HD constexpr int combine_bytes(int mb) {
+    return consumer_parities(mb) > 1 ? kSlabs * n8_tiles(mb) * 4 * 32 * 4 : 0;
 }
 
-// Scratch for adding the two K halves of every slab pair at a row block's end.
-QMM_HD constexpr int reduce_scratch_bytes(int mb) { return kSlabPairs * kSPW * n8_tiles(mb) * 4 * 32 * 4; }
-// Dynamic shared memory of the main kernel with `stages` pipeline stages.
-// (1024 bytes of slack let the kernel align its stage ring to 1024.)
-QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int stages) {
-    return 1024 + stages * stage_bytes(bits, group, mb) + stages * 16 + reduce_scratch_bytes(mb);
+// Dynamic shared memory of the main kernel with S weight stages and F
+// activation slots: the stages, the slots, two mbarriers per weight stage
+// (landed, consumed), per activation slot one per tile (raw landed) and two
+// more (staged, consumed), and the combine scratch. 1024 bytes of slack let the kernel align
+// its rings to 1024.
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int S, int F) {
+    return 1024 + S * wstage_bytes(bits, group) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
+           combine_bytes(mb);
 }
-
+// The most weight stages (<= kMaxStages) that fit kSmemOptin next to F
+// activation slots, a multiple of the consumer parities (each parity owns the
+// stages of its parity); 0 if fewer than two fit.
+QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, int F) {
+    return (main_smem_bytes(bits, group, mb, 8, F) <= kSmemOptin   ? 8
+          : main_smem_bytes(bits, group, mb, 7, F) <= kSmemOptin ? 7
+          : main_smem_bytes(bits, group, mb, 6, F) <= kSmemOptin ? 6
+          : main_smem_bytes(bits, group, mb, 5, F) <= kSmemOptin ? 5
+          : main_smem_bytes(bits, group, mb, 4, F) <= kSmemOptin ? 4
+          : main_smem_bytes(bits, group, mb, 3, F) <= kSmemOptin ? 3
+          : main_smem_bytes(bits, group, mb, 2, F) <= kSmemOptin ? 2
+                                                                     : 0) /
+           consumer_parities(mb) * consumer_parities(mb);
+}
+// Activation slots: a multiple of the consumer parities, and for the 8-row
+// kernel as many as its staging warps per tile (one each); the larger choice
+// when it still leaves four weight stages.
+QMM_HD constexpr int act_slots(int bits, int group, int mb) {
+    return mb == 8 ? (weight_stages_for(bits, group, mb, 6) >= 4   ? 6
+                      : weight_stages_for(bits, group, mb, 4) >= 4 ? 4
+                                                                   : 2)
+                   : (weight_stages_for(bits, group, mb, 4) >= 4 ? 4 : 2);
+}
+QMM_HD constexpr int stage_count(int bits, int group, int mb) {
+    return weight_stages_for(bits, group, mb, act_slots(bits, group, mb));
+}
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb) {
+    return main_smem_bytes(bits, group, mb, stage_count(bits, group, mb), act_slots(bits, group, mb));
+}
 
 }  // namespace qmmk

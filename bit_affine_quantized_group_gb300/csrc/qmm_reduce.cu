@@ -7,7 +7,10 @@
 namespace qmmk {
 
 __global__ void __launch_bounds__(kReduceThreads) qmm_splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
-    griddep_wait();   // partials of the main kernel are complete and visible
+    // the next kernel on the stream may be scheduled now; the partials of the
+    // main kernel are complete and visible after the wait
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t per_bank = static_cast<int64_t>(p.M) * p.N;
     const int64_t total = per_bank * (p.swiglu ? 1 : p.banks);
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;

@@ -78,7 +78,7 @@ def test_workspace_bytes(q):
     d = q.make_desc(**GOOD)
     n = q.workspace_bytes(d)
     assert n > 0
-    # splits = 1: only the activation staging (20 chunks of 16-row fragments), no partials
+    # splits = 1: only the error word (activations are staged in shared memory)
     n1 = q.workspace_bytes(q.make_desc(**{**GOOD, "splits": 1}))
     assert 0 < n1 < 1024 * 1024
     # splits = 0 (automatic) is sized for the largest automatic choice (here 20 chunks / 3 = 6)
@@ -101,6 +101,7 @@ def _args(**kw):
     ({"M": 0, "x": 0}, 0),                      # M = 0: no-op, x may be NULL
     ({"M": -1}, 1), ({"M": 17}, 1),
     ({"x": 0}, 1), ({"x": 0x1001}, 1),          # NULL / misaligned bf16
+    ({"x": 0x1008}, 1),                         # x rows are bulk-copied: 16-byte alignment
     ({"w": [0]}, 1), ({"w": [0x2008]}, 1),      # packed rows need 16-byte alignment
     ({"s": [0x3004]}, 1), ({"b": [0]}, 1),      # G % 8 == 0 -> scales/biases 16-byte aligned
     ({"out": [0x5002]}, 0),                     # bf16 out: 2-byte alignment is enough
