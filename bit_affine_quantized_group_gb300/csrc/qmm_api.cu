@@ -19,11 +19,12 @@ struct qmm_plan {
     qmm_desc d;
     int device;
     int num_sms;
+    int optin;           // opt-in shared memory per CTA
     int splits;
     int C;
     int G;
-    int stages[2];       // index 0: M <= 8 (MB = 8), 1: M > 8 (MB = 16)
-    int smem[2];
+    int stages[3];       // index 0: M <= 8 (MB = 8, narrow), 1: M > 8 (MB = 16), 2: M <= 8 wide (0: not usable)
+    int smem[3];
     uint8_t* ws;
     size_t ws_bytes;
     bool owns_ws;
@@ -36,6 +37,16 @@ struct qmm_plan {
 namespace {
 
 constexpr size_t kErrBytes = 256;
+
+// Index into the plan's stages/smem of the main kernel that a call of M rows
+// over rows_total flattened rows (banks x slices x N) launches.
+int layout_index(const struct qmm_plan* p, int M, int64_t rows_total) {
+    if (M > 8) return 1;
+    if (p->stages[2] == 0) return 0;
+    int64_t ctas = (rows_total + kSlab - 1) / kSlab;
+    if (ctas > p->num_sms) ctas = p->num_sms;
+    return wide_layout(p->d.bits, p->d.group, 8, rows_total, ctas, p->optin) ? 2 : 0;
+}
 
 int chunks_of(const qmm_desc* d) {
     const int64_t G = d->K / d->group;
@@ -56,7 +67,6 @@ int auto_splits(const qmm_desc* d, int num_sms) {
                             splits_cap(d));
 }
 
-int mb_index(int M) { return M > 8 ? 1 : 0; }
 
 size_t partial_region_bytes(const qmm_desc* d, int splits) {
     // unsliced plans with two or more banks keep room for the fused gate/up
@@ -149,21 +159,24 @@ int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_by
     p->splits = d->splits > 0 ? d->splits : auto_splits(d, sms);
     if (p->splits > splits_cap(d)) p->splits = splits_cap(d);
 
-    const int nmb = d->max_M > 8 ? 2 : 1;
-    for (int i = 0; i < 2; ++i) {
+    p->optin = optin;
+    for (int i = 0; i < 3; ++i) {
         p->stages[i] = 0;
         p->smem[i] = 0;
     }
-    for (int i = 0; i < nmb; ++i) {
-        const int mb = i == 0 ? 8 : 16;
-        const int st = stages_for(d->bits, d->group, mb, optin);
+    for (int i = 0; i < 3; ++i) {
+        const int mb = i == 1 ? 16 : 8;
+        const bool wide = i == 2;
+        if (mb == 16 && d->max_M <= 8) continue;
+        const int st = stages_for(d->bits, d->group, mb, wide, optin);
         if (st < 2) {
+            if (wide) continue;   // the narrow layout serves every call
             delete p;
             return QMM_ERR_UNSUPPORTED;
         }
         p->stages[i] = st;
-        p->smem[i] = main_smem_bytes(d->bits, d->group, mb);
-        if (configure_format(d->bits, d->group, mb, p->smem[i]) != cudaSuccess) {
+        p->smem[i] = main_smem_bytes(d->bits, d->group, mb, wide);
+        if (configure_format(d->bits, d->group, mb, wide, p->smem[i]) != cudaSuccess) {
             delete p;
             return QMM_ERR_CUDA;
         }
@@ -198,9 +211,10 @@ int qmm_plan_get_info(const qmm_plan_t* p, qmm_plan_info* info) {
     if (p == nullptr || info == nullptr) return QMM_ERR_INVALID_ARG;
     info->splits = p->splits;
     info->chunks = p->C;
-    info->stages[0] = p->stages[0];
+    const int l8 = layout_index(p, 1, static_cast<int64_t>(p->splits) * p->d.N);
+    info->stages[0] = p->stages[l8];
     info->stages[1] = p->stages[1];
-    info->smem_bytes[0] = p->smem[0];
+    info->smem_bytes[0] = p->smem[l8];
     info->smem_bytes[1] = p->smem[1];
     info->num_sms = p->num_sms;
     info->device = p->device;
@@ -244,7 +258,8 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
     if (chk != QMM_OK) return chk;
     if (M == 0) return QMM_OK;
 
-    const int mi = mb_index(M);
+    const int64_t rows_total = static_cast<int64_t>(swiglu ? 1 : n_banks) * p->splits * N;
+    const int mi = layout_index(p, M, rows_total);
     if (p->stages[mi] == 0) return QMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     struct qmm_plan* mp_plan = const_cast<struct qmm_plan*>(p);   // the tensor-map caches are plan-owned scratch
@@ -265,12 +280,13 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
     h.unpack_magic = kF16x2_1024;
     h.banks = n_banks;
     h.gate = swiglu ? p->partial : nullptr;
-    h.rows_total = static_cast<int64_t>(swiglu ? 1 : n_banks) * p->splits * N;
+    h.rows_total = rows_total;
 
     int64_t ctas = (h.rows_total + kSlab - 1) / kSlab;
     if (ctas > p->num_sms) ctas = p->num_sms;
     LaunchCfg L;
-    L.mb = mi == 0 ? 8 : 16;
+    L.mb = mi == 1 ? 16 : 8;
+    L.wide = mi == 2;
     L.ctas = static_cast<int>(ctas);
     L.smem = p->smem[mi];
     L.stream = st;

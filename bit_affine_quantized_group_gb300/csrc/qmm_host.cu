@@ -7,9 +7,20 @@
 
 namespace qmmk {
 
-int stages_for(int bits, int group, int mb, int optin) {
-    const int st = stage_count(bits, group, mb);
-    return (st >= 2 && main_smem_bytes(bits, group, mb) <= optin) ? st : 0;
+int stages_for(int bits, int group, int mb, bool wide, int optin) {
+    if (wide && mb != 8) return 0;
+    const int st = stage_count(bits, group, mb, wide);
+    return (st >= 2 && main_smem_bytes(bits, group, mb, wide) <= optin) ? st : 0;
+}
+
+// A wide consumer warp owns two slabs of each row block: with CTA row ranges of
+// fewer than 96 rows some wide warps would idle while others carry two slabs,
+// and with fewer than four weight stages each parity would wait for its own
+// refills; the narrow layout (every warp on every item) is then faster.
+bool wide_layout(int bits, int group, int mb, int64_t rows_total, int64_t ctas, int optin) {
+    if (mb != 8 || ctas < 1) return false;
+    if (stages_for(bits, group, 8, true, optin) < 4) return false;
+    return rows_total / ctas >= 96;
 }
 
 int chunk_count(int64_t K, int group) { return static_cast<int>((K / group + kGPC - 1) / kGPC); }
@@ -47,14 +58,14 @@ int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, i
     return best;
 }
 
-cudaError_t configure_format(int bits, int group, int mb, int smem_bytes) {
+cudaError_t configure_format(int bits, int group, int mb, bool wide, int smem_bytes) {
     switch (bits) {
-        case 2: return configure_kernels<2>(group, mb, smem_bytes);
-        case 3: return configure_kernels<3>(group, mb, smem_bytes);
-        case 4: return configure_kernels<4>(group, mb, smem_bytes);
-        case 5: return configure_kernels<5>(group, mb, smem_bytes);
-        case 6: return configure_kernels<6>(group, mb, smem_bytes);
-        case 8: return configure_kernels<8>(group, mb, smem_bytes);
+        case 2: return configure_kernels<2>(group, mb, wide, smem_bytes);
+        case 3: return configure_kernels<3>(group, mb, wide, smem_bytes);
+        case 4: return configure_kernels<4>(group, mb, wide, smem_bytes);
+        case 5: return configure_kernels<5>(group, mb, wide, smem_bytes);
+        case 6: return configure_kernels<6>(group, mb, wide, smem_bytes);
+        case 8: return configure_kernels<8>(group, mb, wide, smem_bytes);
         default: return cudaErrorInvalidValue;
     }
 }

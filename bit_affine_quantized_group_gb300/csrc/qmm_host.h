@@ -11,9 +11,16 @@
 
 namespace qmmk {
 
-// The format's pipeline depth (stage_count, fixed at compile time) when its
-// main-kernel shared memory fits `optin` bytes; 0 otherwise.
-int stages_for(int bits, int group, int mb, int optin);
+// The format's pipeline depth (stage_count, fixed at compile time) for a row
+// tile and consumer layout when its main-kernel shared memory fits `optin`
+// bytes; 0 otherwise.
+int stages_for(int bits, int group, int mb, bool wide, int optin);
+
+// Consumer layout of a call's main kernel: wide (two slabs a warp, two
+// parities; 8-row kernel only) when the CTAs' row ranges fill most of a
+// 128-row block and the wide layout keeps at least four weight stages;
+// narrow otherwise.
+bool wide_layout(int bits, int group, int mb, int64_t rows_total, int64_t ctas, int optin);
 
 // 8-group chunks along K.
 int chunk_count(int64_t K, int group);
@@ -22,8 +29,9 @@ int chunk_count(int64_t K, int group);
 // format on `num_sms` SMs, from a per-CTA cost model (see qmm_host.cu).
 int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, int num_sms, int cap);
 
-// Set the main kernels' dynamic shared-memory limit for one format and row tile.
-cudaError_t configure_format(int bits, int group, int mb, int smem_bytes);
+// Set the main kernels' dynamic shared-memory limit for one format, row tile
+// and consumer layout.
+cudaError_t configure_format(int bits, int group, int mb, bool wide, int smem_bytes);
 
 // Launch the main kernel of one format (exactly one of the parameter blocks is non-null).
 cudaError_t launch_format(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,

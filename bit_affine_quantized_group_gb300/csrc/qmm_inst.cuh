@@ -7,19 +7,19 @@
 namespace qmmk {
 
 namespace {
-template <int BITS, int GROUP, int MB>
+template <int BITS, int GROUP, int MB, bool WIDE>
 cudaError_t configure_one(int smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 1>,
+    cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 1, WIDE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 2, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, kMaxBanks>,
+    return cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, kMaxBanks, WIDE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
 }
 
-template <int BITS, int GROUP, int MB, int CAP>
+template <int BITS, int GROUP, int MB, int CAP, bool WIDE>
 cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     // The main kernel is a programmatic dependent of whatever precedes it on the
     // stream: it is scheduled as soon as that work allows (its CTAs take SMs as
@@ -36,23 +36,38 @@ cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     cfg.stream = L.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP>, mp);
+    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP, WIDE>, mp);
 }
 
-template <int BITS, int GROUP, int MB>
+template <int BITS, int GROUP, int MB, bool WIDE>
 cudaError_t launch_cap(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked,
                        const MainParams<2>* fused) {
-    if (single) return launch_one<BITS, GROUP, MB, 1>(L, *single);
-    if (fused) return launch_one<BITS, GROUP, MB, 2>(L, *fused);
-    return launch_one<BITS, GROUP, MB, kMaxBanks>(L, *banked);
+    if (single) return launch_one<BITS, GROUP, MB, 1, WIDE>(L, *single);
+    if (fused) return launch_one<BITS, GROUP, MB, 2, WIDE>(L, *fused);
+    return launch_one<BITS, GROUP, MB, kMaxBanks, WIDE>(L, *banked);
+}
+
+template <int BITS, int GROUP>
+cudaError_t configure_group(int mb, bool wide, int smem_bytes) {
+    if (mb == 16) return wide ? cudaErrorInvalidValue : configure_one<BITS, GROUP, 16, false>(smem_bytes);
+    return wide ? configure_one<BITS, GROUP, 8, true>(smem_bytes) : configure_one<BITS, GROUP, 8, false>(smem_bytes);
+}
+
+template <int BITS, int GROUP>
+cudaError_t launch_group(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked,
+                         const MainParams<2>* fused) {
+    if (L.mb == 16)
+        return L.wide ? cudaErrorInvalidValue : launch_cap<BITS, GROUP, 16, false>(L, single, banked, fused);
+    return L.wide ? launch_cap<BITS, GROUP, 8, true>(L, single, banked, fused)
+                  : launch_cap<BITS, GROUP, 8, false>(L, single, banked, fused);
 }
 }  // namespace
 
 template <>
-cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, int smem_bytes) {
+cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, bool wide, int smem_bytes) {
     constexpr int B = QMM_INST_BITS;
-    if (group == 32) return mb == 8 ? configure_one<B, 32, 8>(smem_bytes) : configure_one<B, 32, 16>(smem_bytes);
-    if (group == 64) return mb == 8 ? configure_one<B, 64, 8>(smem_bytes) : configure_one<B, 64, 16>(smem_bytes);
+    if (group == 32) return configure_group<B, 32>(mb, wide, smem_bytes);
+    if (group == 64) return configure_group<B, 64>(mb, wide, smem_bytes);
     return cudaErrorInvalidValue;
 }
 
@@ -60,12 +75,8 @@ template <>
 cudaError_t launch_forward<QMM_INST_BITS>(int group, const LaunchCfg& L, const MainParams<1>* single,
                                           const MainParams<kMaxBanks>* banked, const MainParams<2>* fused) {
     constexpr int B = QMM_INST_BITS;
-    if (group == 32)
-        return L.mb == 8 ? launch_cap<B, 32, 8>(L, single, banked, fused)
-                         : launch_cap<B, 32, 16>(L, single, banked, fused);
-    if (group == 64)
-        return L.mb == 8 ? launch_cap<B, 64, 8>(L, single, banked, fused)
-                         : launch_cap<B, 64, 16>(L, single, banked, fused);
+    if (group == 32) return launch_group<B, 32>(L, single, banked, fused);
+    if (group == 64) return launch_group<B, 64>(L, single, banked, fused);
     return cudaErrorInvalidValue;
 }
 

@@ -213,12 +213,13 @@ __device__ __forceinline__ int wtile_off(int r, int b) {
 // ---------------------------------------------------------------------------
 // The main kernel.
 // ---------------------------------------------------------------------------
-template <int BITS, int GROUP, int MB, int CAP>
+template <int BITS, int GROUP, int MB, int CAP, bool WIDE>
 __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
     constexpr int NT = n8_tiles(MB);
     constexpr int NSW = staging_warps(MB);
-    constexpr int NCW = consumer_warps(MB);
-    constexpr int CPAR = consumer_parities(MB);
+    static_assert(MB == 8 || !WIDE, "the wide consumer layout is for the 8-row kernel");
+    constexpr int NCW = consumer_warps();
+    constexpr int CPAR = consumer_parities(WIDE);
     constexpr int WPPC = NCW / CPAR;             // consumer warps of one parity
     constexpr int VB = vblocks_per_group(GROUP);
     constexpr int VPC = vblocks_per_chunk(GROUP);
@@ -251,8 +252,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
     // array so every access below stays a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    constexpr int S = stage_count(BITS, GROUP, MB);     // weight stages
-    constexpr int F = act_slots(BITS, GROUP, MB);       // activation slots
+    constexpr int S = stage_count(BITS, GROUP, MB, WIDE);     // weight stages
+    constexpr int F = act_slots(BITS, GROUP, MB, WIDE);       // activation slots
     static_assert(S >= 2 && F >= 2 && S % CPAR == 0 && F % CPAR == 0, "pipeline depth");
     uint8_t* aring = smem + S * WSB;                                        // activation slots
     uint64_t* wfull = reinterpret_cast<uint64_t*>(aring + F * ASB);        // weights, scales, biases landed
@@ -639,7 +640,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     // chunks in the stage slots of parity cp (all slots when CPAR == 1). The
     // slabs of a warp share its activation fragment loads and give it SPW
     // independent MMA chains.
-    constexpr int SPW = consumer_slabs(MB);
+    constexpr int SPW = consumer_slabs(WIDE);
     constexpr int WPP = kSlabs / SPW;            // consumer warps per parity
     const int w = warp % WPP;
     const int cp = warp / WPP;
@@ -1015,13 +1016,16 @@ __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restr
 // ---------------------------------------------------------------------------
 struct LaunchCfg {
     int mb;            // 8 or 16
+    bool wide;         // consumer layout (8-row kernel only)
     int ctas;
     int smem;
     cudaStream_t stream;
 };
 
+// Set the dynamic shared-memory limit of one format's main kernels for one row
+// tile and consumer layout (every bank capacity).
 template <int BITS>
-cudaError_t configure_kernels(int group, int mb, int smem_bytes);
+cudaError_t configure_kernels(int group, int mb, bool wide, int smem_bytes);
 
 // Weight-box width for a format (host side, for encoding tensor maps).
 inline int weight_box_width(int bits, int group) { return wbox_width(bits, group); }

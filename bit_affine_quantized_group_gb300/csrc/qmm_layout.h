@@ -51,16 +51,18 @@ QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
 // tile owning the activation slots s with s % staging_per_tile == p.
 QMM_HD constexpr int staging_per_tile(int mb) { return mb == 8 ? 6 : 2; }
 QMM_HD constexpr int staging_warps(int mb) { return staging_per_tile(mb) * n8_tiles(mb); }
-// Consumer warps: consumer_slabs(mb) 16-row slabs per warp, one warp per slab
-// group and consumer parity. The 8-row kernel gives a warp two slabs (two
-// independent MMA chains sharing the activation fragment loads) and runs two
-// parities; the 16-row kernel's wider fragments need the registers of one slab
-// and one parity. Either way 8 consumer warps; with the staging warps and the
-// producer at most four warps share a scheduler, so 128 registers a thread.
-QMM_HD constexpr int consumer_slabs(int mb) { return mb == 8 ? 2 : 1; }
-QMM_HD constexpr int consumer_parities(int mb) { return mb == 8 ? 2 : 1; }
-QMM_HD constexpr int consumer_warps(int mb) { return kSlabs / consumer_slabs(mb) * consumer_parities(mb); }
-QMM_HD constexpr int main_threads(int mb) { return (consumer_warps(mb) + staging_warps(mb) + 1) * 32; }
+// Consumer warps, in one of two layouts, 8 warps either way (with the staging
+// warps and the producer at most four warps share a scheduler: 128 registers a
+// thread):
+//   * narrow: one 16-row slab a warp, every work item;
+//   * wide (8-row kernel only): two slabs a warp (two independent MMA chains
+//     sharing the activation fragment loads) in two parities, parity p taking
+//     the items in the stage slots of parity p. It pays when a CTA's row blocks
+//     fill most of the 8 slabs and the pipeline keeps several stages per parity.
+QMM_HD constexpr int consumer_slabs(bool wide) { return wide ? 2 : 1; }
+QMM_HD constexpr int consumer_parities(bool wide) { return wide ? 2 : 1; }
+QMM_HD constexpr int consumer_warps() { return kSlabs; }
+QMM_HD constexpr int main_threads(int mb) { return (consumer_warps() + staging_warps(mb) + 1) * 32; }
 
 // k32 blocks per scale group and per chunk.
 QMM_HD constexpr int vblocks_per_group(int group) { return group / 32; }
@@ -109,48 +111,46 @@ QMM_HD constexpr int wstage_bytes(int bits, int group) {
 QMM_HD constexpr int aslot_bytes(int group, int mb) { return round_up(xraw_bytes(group, mb) + xstaged_bytes(group, mb), 1024); }
 
 // Scratch for adding the second consumer parity's partial sums at the end of
-// a row block: [slab][tile][4][32 lanes] floats.
-QMM_HD constexpr int combine_bytes(int mb) {
-    return consumer_parities(mb) > 1 ? kSlabs * n8_tiles(mb) * 4 * 32 * 4 : 0;
-}
+// a row block (wide layout): [slab][tile][4][32 lanes] floats.
+QMM_HD constexpr int combine_bytes(int mb, bool wide) { return wide ? kSlabs * n8_tiles(mb) * 4 * 32 * 4 : 0; }
 
 // Dynamic shared memory of the main kernel with S weight stages and F
 // activation slots: the stages, the slots, two mbarriers per weight stage
 // (landed, consumed), per activation slot one per tile (raw landed) and two
 // more (staged, consumed), and the combine scratch. 1024 bytes of slack let the kernel align
 // its rings to 1024.
-QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int S, int F) {
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, bool wide, int S, int F) {
     return 1024 + S * wstage_bytes(bits, group) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
-           combine_bytes(mb);
+           combine_bytes(mb, wide);
 }
 // The most weight stages (<= kMaxStages) that fit kSmemOptin next to F
 // activation slots, a multiple of the consumer parities (each parity owns the
 // stages of its parity); 0 if fewer than two fit.
-QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, int F) {
-    return (main_smem_bytes(bits, group, mb, 8, F) <= kSmemOptin   ? 8
-          : main_smem_bytes(bits, group, mb, 7, F) <= kSmemOptin ? 7
-          : main_smem_bytes(bits, group, mb, 6, F) <= kSmemOptin ? 6
-          : main_smem_bytes(bits, group, mb, 5, F) <= kSmemOptin ? 5
-          : main_smem_bytes(bits, group, mb, 4, F) <= kSmemOptin ? 4
-          : main_smem_bytes(bits, group, mb, 3, F) <= kSmemOptin ? 3
-          : main_smem_bytes(bits, group, mb, 2, F) <= kSmemOptin ? 2
-                                                                     : 0) /
-           consumer_parities(mb) * consumer_parities(mb);
+QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, bool wide, int F) {
+    return (main_smem_bytes(bits, group, mb, wide, 8, F) <= kSmemOptin   ? 8
+          : main_smem_bytes(bits, group, mb, wide, 7, F) <= kSmemOptin ? 7
+          : main_smem_bytes(bits, group, mb, wide, 6, F) <= kSmemOptin ? 6
+          : main_smem_bytes(bits, group, mb, wide, 5, F) <= kSmemOptin ? 5
+          : main_smem_bytes(bits, group, mb, wide, 4, F) <= kSmemOptin ? 4
+          : main_smem_bytes(bits, group, mb, wide, 3, F) <= kSmemOptin ? 3
+          : main_smem_bytes(bits, group, mb, wide, 2, F) <= kSmemOptin ? 2
+                                                                        : 0) /
+           consumer_parities(wide) * consumer_parities(wide);
 }
-// Activation slots: a multiple of the consumer parities, and for the 8-row
-// kernel as many as its staging warps per tile (one each); the larger choice
-// when it still leaves four weight stages.
-QMM_HD constexpr int act_slots(int bits, int group, int mb) {
-    return mb == 8 ? (weight_stages_for(bits, group, mb, 6) >= 4   ? 6
-                      : weight_stages_for(bits, group, mb, 4) >= 4 ? 4
-                                                                   : 2)
-                   : (weight_stages_for(bits, group, mb, 4) >= 4 ? 4 : 2);
+// Activation slots: a multiple of the consumer parities, and either at most
+// the staging warps per tile or a multiple of them (each warp owns whole
+// slots); the larger choice when it still leaves four weight stages.
+QMM_HD constexpr int act_slots(int bits, int group, int mb, bool wide) {
+    return mb == 8 ? (weight_stages_for(bits, group, mb, wide, 6) >= 4   ? 6
+                      : weight_stages_for(bits, group, mb, wide, 4) >= 4 ? 4
+                                                                         : 2)
+                   : (weight_stages_for(bits, group, mb, wide, 4) >= 4 ? 4 : 2);
 }
-QMM_HD constexpr int stage_count(int bits, int group, int mb) {
-    return weight_stages_for(bits, group, mb, act_slots(bits, group, mb));
+QMM_HD constexpr int stage_count(int bits, int group, int mb, bool wide) {
+    return weight_stages_for(bits, group, mb, wide, act_slots(bits, group, mb, wide));
 }
-QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb) {
-    return main_smem_bytes(bits, group, mb, stage_count(bits, group, mb), act_slots(bits, group, mb));
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, bool wide) {
+    return main_smem_bytes(bits, group, mb, wide, stage_count(bits, group, mb, wide), act_slots(bits, group, mb, wide));
 }
 
 }  // namespace qmmk

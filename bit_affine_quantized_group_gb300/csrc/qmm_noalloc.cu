@@ -45,7 +45,7 @@ struct DeviceSetup {
     uint8_t* scratch;         // device address of g_noalloc_scratch on this device
     int num_sms;
     int optin;
-    uint32_t configured;      // bit (bits_index * 4 + group_index * 2 + mb_index): kernel attributes set
+    uint64_t configured;      // bit (bits_index * 6 + group_index * 3 + layout): kernel attributes set
 };
 
 DeviceSetup g_dev[kMaxDevices];
@@ -81,9 +81,11 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     const int mb = M > 8 ? 16 : 8;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_ERR_CUDA;
-    const uint32_t cfg_bit = 1u << (bits_index(bits) * 4 + (group == 64 ? 2 : 0) + (mb == 16 ? 1 : 0));
     DeviceSetup ds;
     int stages = 0;
+    bool wide = false;
+    int splits = 1;
+    const int C = chunk_count(K, group);
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         DeviceSetup& s = g_dev[dev];
@@ -100,24 +102,29 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
             s.configured = 0;
             s.ready = true;
         }
-        stages = stages_for(bits, group, mb, s.optin);
+        // 3. K slices: the automatic choice, lowered until the partial sums fit;
+        //    then the consumer layout, as qmm_forward chooses it.
+        int cap = C / 2;
+        if (cap < 1) cap = 1;
+        if (cap > 8) cap = 8;
+        splits = auto_split_count(K, N, bits, group, 1, s.num_sms, cap);
+        const size_t per_split = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+        while (splits > 1 && kErrArea + static_cast<size_t>(splits) * per_split > QMM_NOALLOC_SCRATCH_BYTES) --splits;
+        const int64_t rows = static_cast<int64_t>(splits) * N;
+        int64_t ctas = (rows + kSlab - 1) / kSlab;
+        if (ctas > s.num_sms) ctas = s.num_sms;
+        wide = wide_layout(bits, group, mb, rows, ctas, s.optin);
+        stages = stages_for(bits, group, mb, wide, s.optin);
         if (stages < 2) return QMM_ERR_UNSUPPORTED;
+        const int layout = mb == 16 ? 1 : (wide ? 2 : 0);
+        const uint64_t cfg_bit = 1ull << (bits_index(bits) * 6 + (group == 64 ? 3 : 0) + layout);
         if (!(s.configured & cfg_bit)) {
-            if (configure_format(bits, group, mb, main_smem_bytes(bits, group, mb)) != cudaSuccess)
+            if (configure_format(bits, group, mb, wide, main_smem_bytes(bits, group, mb, wide)) != cudaSuccess)
                 return QMM_ERR_CUDA;
             s.configured |= cfg_bit;
         }
         ds = s;
     }
-
-    // 3. K slices: the automatic choice, lowered until the partial sums fit.
-    const int C = chunk_count(K, group);
-    int cap = C / 2;
-    if (cap < 1) cap = 1;
-    if (cap > 8) cap = 8;
-    int splits = auto_split_count(K, N, bits, group, 1, ds.num_sms, cap);
-    const size_t per_split = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
-    while (splits > 1 && kErrArea + static_cast<size_t>(splits) * per_split > QMM_NOALLOC_SCRATCH_BYTES) --splits;
 
     // 4. Launch the kernels qmm_forward launches, pointed at the scratch.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -154,8 +161,9 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     if (ctas > ds.num_sms) ctas = ds.num_sms;
     LaunchCfg L;
     L.mb = mb;
+    L.wide = wide;
     L.ctas = static_cast<int>(ctas);
-    L.smem = main_smem_bytes(bits, group, mb);
+    L.smem = main_smem_bytes(bits, group, mb, wide);
     L.stream = st;
     if (launch_format(bits, group, L, &mp, nullptr, nullptr) != cudaSuccess) return QMM_ERR_CUDA;
     if (splits > 1) {

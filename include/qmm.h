@@ -30,9 +30,10 @@
  * performance and parity receipt", MTPLX logic review, and the "JANGH split-K
  * verify tile" commit tests 2/4/8-bit codes; 3-bit follows the same stream.)
  * Requirements checked before any launch: K % group == 0; K*bits % 128 == 0
- * (every packed row starts on a 16-byte boundary); K/group even; packed
- * weights, scales and biases 16-byte aligned device pointers; x and out
- * naturally aligned device pointers.
+ * (every packed row starts on a 16-byte boundary); K/group even (so K is a
+ * multiple of 64); x, packed weights, scales and biases 16-byte aligned
+ * device pointers (x is read with tensor-memory-access copies); out a
+ * naturally aligned device pointer.
  *
  * Split-K (same page, commit "JANGH split-K verify tile": K is sliced across
  * the grid, FP32 partials are written and then summed): with splits S > 1 the
@@ -73,7 +74,7 @@ enum {
     QMM_ERR_CUDA = 4,          /* a CUDA runtime call failed (no device, launch error) */
     QMM_ERR_ALLOC = 5,         /* host or device allocation failed in qmm_plan */
     QMM_ERR_TIMEOUT = 6,       /* a kernel gave up a bounded wait (qmm_plan_error) */
-    QMM_ERR_SCRATCH_LIMIT = 7  /* qmm_forward_noalloc: the call needs more than its static scratch */
+    QMM_ERR_SCRATCH_LIMIT = 7  /* reserved (no longer returned: qmm_forward_noalloc lowers its K slices to fit) */
 };
 
 /* Output element types. */
@@ -99,7 +100,8 @@ typedef struct qmm_desc {
 typedef struct qmm_plan_info {
     int32_t splits;          /* K slices used by every forward call */
     int32_t chunks;          /* 8-group chunks along K */
-    int32_t stages[2];       /* pipeline depth for M <= 8 and for 9 <= M <= 16 */
+    int32_t stages[2];       /* weight-pipeline depth of the main kernel a single-projection call
+                                of M <= 8 rows uses, and of the one for 9 <= M <= 16 */
     int32_t smem_bytes[2];   /* dynamic shared memory per CTA, same order */
     int32_t num_sms;         /* streaming multiprocessors on the plan's device */
     int32_t device;          /* CUDA device ordinal the plan was made on */
@@ -118,10 +120,11 @@ typedef struct qmm_plan qmm_plan_t;
 int qmm_validate_desc(const qmm_desc* d);
 
 /*
- * Device workspace a plan for `d` needs (bytes; 0 if d is invalid): the
- * per-call activation staging area plus split-K partials for
- * max_banks * splits * max_M * N floats (splits = 0 is sized for the largest
- * automatic choice, min(8, chunks / 2) with chunks = ceil(K / group / 8)). Lets the caller (e.g. PyTorch's allocator) own it.
+ * Device workspace a plan for `d` needs (bytes; 0 if d is invalid): a
+ * 256-byte error word plus split-K partials for max_banks * splits * max_M * N
+ * floats (splits = 0 is sized for the largest automatic choice,
+ * min(8, chunks / 2) with chunks = ceil(K / group / 8)). Lets the caller
+ * (e.g. PyTorch's allocator) own it.
  */
 size_t qmm_workspace_bytes(const qmm_desc* d);
 
@@ -155,8 +158,9 @@ int qmm_check_forward_args(const qmm_desc* d, const void* x_bf16, int M, int n_b
  * y = qmm(x, w, scales, biases) for one projection. M = 0 is a no-op that
  * returns QMM_OK. K, N, bits and group must equal the plan's
  * (QMM_ERR_PLAN_MISMATCH otherwise); M must be <= the plan's max_M.
- * Launches, in stream order: an activation-staging kernel, the main kernel
- * and, when the plan's splits > 1, the split-K reduce kernel.
+ * Launches, in stream order: the main kernel (it streams the weights, stages
+ * the activations and computes the projection) and, when the plan's
+ * splits > 1, the split-K reduce kernel.
  *
  * Ordering: x is read only after the work issued before the call on the
  * stream has finished, and out is written after that too. The packed weights,
@@ -234,14 +238,15 @@ int qmm_plan_error(const qmm_plan_t* p, uint32_t* flags);
  * after start-up, plug-in hosts that only hand over their tensors). The pages
  * describe no counterpart: this is a deployment variant of qmm_forward.
  *
- * Same arguments and data layout as qmm_forward, with the output type given
- * directly (QMM_OUT_F32 or QMM_OUT_BF16) and splits fixed at 1. The per-call
- * activation staging lives in a static device array of
- * QMM_NOALLOC_SCRATCH_BYTES; a call whose staging would not fit returns
- * QMM_ERR_SCRATCH_LIMIT before touching the device. The staging size does not
- * depend on the code width: with 9..16 rows the largest K is 114688 in groups
- * of 32 and 122368 in groups of 64; with 1..8 rows 229632 and 244736. Nothing
- * is allocated: no cudaMalloc, no cudaFree, no allocating library routine.
+ * Same arguments, data layout and kernels as qmm_forward, with the output
+ * type given directly (QMM_OUT_F32 or QMM_OUT_BF16). The device scratch that
+ * qmm_forward keeps in its plan's workspace (the kernels' error word and the
+ * fp32 partial sums of K slices) lives in a static device array of
+ * QMM_NOALLOC_SCRATCH_BYTES. The K-slice count is the one an automatic plan
+ * would choose, lowered until 256 + slices * M * N * 4 bytes fit the array
+ * (one slice needs no partials), so every supported shape runs; results are
+ * bitwise those of qmm_forward with a plan of that slice count. Nothing is
+ * allocated: no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * The first call on a device (with that device current) looks up the
  * scratch's device address and sets the kernels' shared-memory limit; make
