@@ -131,9 +131,14 @@ struct WorkIter {
     int64_t n0;             // first weight row of the current row block
     bool valid;
 
+    // The CTAs split the flattened rows on the 16-row slab grid (a CTA holds
+    // whole slabs, the last one of the range possibly ragged), and a CTA walks
+    // its part of a segment in blocks of kTN rows (the last one shorter): the
+    // consumers then compute few empty slab rows.
     __device__ __forceinline__ void init(const MainHeader& p) {
-        r = p.rows_total * blockIdx.x / gridDim.x;
-        r_end = p.rows_total * (blockIdx.x + 1) / gridDim.x;
+        const int64_t slabs = (p.rows_total + kSlab - 1) / kSlab;
+        r = min(p.rows_total, kSlab * (slabs * blockIdx.x / gridDim.x));
+        r_end = min(p.rows_total, kSlab * (slabs * (blockIdx.x + 1) / gridDim.x));
         start_segment(p);
     }
     __device__ __forceinline__ void start_segment(const MainHeader& p) {
@@ -152,8 +157,8 @@ struct WorkIter {
         start_block(p);
     }
     __device__ __forceinline__ void start_block(const MainHeader& p) {
-        const int64_t a = a0 + len * ib / nb;
-        const int64_t e = a0 + len * (ib + 1) / nb;
+        const int64_t a = a0 + static_cast<int64_t>(kTN) * ib;
+        const int64_t e = min(a0 + len, a + kTN);
         n0 = a - seg * p.N;
         rows = static_cast<int>(e - a);
         bank = SWIGLU ? pass : static_cast<int>(seg / p.splits);
