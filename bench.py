@@ -14,7 +14,8 @@ measured HBM peak for the other named configurations, each over rotating device
 copies of its weights larger than L2 and timed by CUDA-graph replay: pr1_ref
 (M=1, 2048 x 2048, 4-bit g64, fp32 out; also with direct stream launches),
 down_longk (17408 -> 5120, 4-bit g64, splits 1/2/4/8/automatic x M 1/8/16),
-mixed_widths (5120 -> 6144, 5/6/8-bit g32, M=8) and banked (36 banks of
+mixed_widths (5120 -> 6144, 5/6/8-bit g32, M=8), the 4/5/6/8-bit widths on the
+mlp_up shape (M=8) and banked (36 banks of
 2048 -> 8192, 4-bit g64, M 1 and 16, per bank set).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qmm|reference]
@@ -295,6 +296,24 @@ def run_per_config(q, peaks, stream):
         assert plan.error_flags() == 0
         del copies, plan
     res["mixed_widths"] = {"workload": "M=8 K=5120 N=6144 g32 bf16 out", **mw}
+
+    # the same code widths on the headline's shape (5120 -> 17408, g32, M=8), so
+    # that the odd widths compare with 4-bit codes at equal problem size
+    ws_ = {}
+    for bits in (4, 5, 6, 8):
+        x, copies, (K, N, group) = _dev_copies("mlp_up", bits, 8)
+        plan = q.Plan(K, N, bits, group, max_M=8, out_dtype="bf16", splits=0)
+        out = torch.empty((8, N), dtype=torch.bfloat16, device=x.device)
+
+        def step_ws():
+            for c in copies:
+                q.forward(plan, x, c[0][0], c[0][1], c[0][2], out, stream=stream)
+        sec = _time_step(step_ws, max(5, 400 // len(copies)), stream) / len(copies)
+        ws_[f"{bits}-bit"] = entry(sec, algorithmic_bytes(8, K, N, bits, group, 2),
+                                   {"splits": plan.info()["splits"], "copies": len(copies)})
+        assert plan.error_flags() == 0
+        del copies, plan
+    res["widths_at_mlp_up_shape"] = {"workload": "M=8 K=5120 N=17408 g32 bf16 out", **ws_}
 
     # banked: 36 x (2048 -> 8192), 4-bit g64, shared x, M 1 and 16, per bank set
     x, sets, (K, N, group) = _dev_copies("banked", 4, 16, banks=36, min_bytes=2 * L2_BYTES)

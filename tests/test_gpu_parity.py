@@ -180,6 +180,40 @@ def test_row_independence(q, oracle_mod, bits, group, splits):
     assert plan.error_flags() == 0
 
 
+@pytest.mark.parametrize("bits", [4, 5, 8])
+def test_consumer_layouts_agree(q, oracle_mod, bits):
+    """The 8-row kernel's two consumer layouts (wide: two slabs a warp in two
+    item parities; narrow: one slab a warp on every item, keeping the even- and
+    odd-item sums apart) add the same terms in the same order. A projection
+    with about 112 rows per CTA takes the wide layout, one with a few rows per
+    CTA the narrow one; on the same weights and x their shared rows must agree
+    bitwise (K spans an even number of 8-group chunks, so each row block's
+    items split the same way), and the narrow result must match the oracle."""
+    import torch
+    K, group = 5120, 32
+    probe = q.Plan(K, 1024, bits, group, max_M=8, out_dtype="f32", splits=1)
+    sms = probe.info()["num_sms"]
+    probe.close()
+    N_wide, N_narrow = sms * 112, 1024
+    inp = datagen.gen_qmm(77 + bits, 8, K, N_wide, bits, group)
+    x, w, s, b = dev_tensors(inp)
+    row_bytes = K * bits // 8
+    G = K // group
+    w_n = w.view(torch.uint8).view(N_wide, row_bytes)[:N_narrow].contiguous().view(torch.int32)
+    s_n, b_n = s.view(N_wide, G)[:N_narrow].contiguous(), b.view(N_wide, G)[:N_narrow].contiguous()
+    plan_w = q.Plan(K, N_wide, bits, group, max_M=8, out_dtype="f32", splits=1)
+    plan_n = q.Plan(K, N_narrow, bits, group, max_M=8, out_dtype="f32", splits=1)
+    for M in (1, 8):
+        y_w = to_f64(run_forward(plan_w, x, w, s, b, M))
+        y_n = to_f64(run_forward(plan_n, x, w_n, s_n, b_n, M))
+        assert np.array_equal(y_w[:, :N_narrow], y_n), (M, np.abs(y_w[:, :N_narrow] - y_n).max())
+        cols = np.arange(0, N_narrow, 7, dtype=np.int64)
+        y_ref = oracle_mod.qmm_f64_cols(inp.x[:M], inp.words[0], inp.scales[0], inp.biases[0], K, N_wide, bits,
+                                        group, cols)
+        check(y_n[:, cols], y_ref, "f32")
+    assert plan_w.error_flags() == 0 and plan_n.error_flags() == 0
+
+
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 def test_activation_dynamic_range(q, oracle_mod, bits):
     """Rows of x at very different magnitudes (2^-110 .. 2^100), a row whose
