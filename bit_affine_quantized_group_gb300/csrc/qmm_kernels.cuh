@@ -7,18 +7,20 @@
 //                            tensor boxes), scales and biases (TMA boxes, or
 //                            4-byte cp.async pieces when a row of them is not
 //                            16-byte aligned) into a ring of shared-memory
-//                            stages from the moment the CTA starts and, once the
-//                            preceding work has finished, the chunk's raw
-//                            activation rows (bulk copies); staging warps turn
-//                            the raw activations into the chunk's tensor-core
-//                            fragments, the per-group activation sums XS (the
-//                            "b*XS" term of the dequant-after-dot form,
-//                            vmlx-swift PR #565, LaneQMM commit) and the range
-//                            factors; eight consumer warps unpack the codes in
-//                            registers and contract them on tensor cores,
-//                            reading each code byte once for all M rows (same
-//                            page, qwen_qmv_rows_full commit: weights read once
-//                            per k-block for all rows).
+//                            weight stages from the moment the CTA starts.
+//                            Once the preceding work has finished, staging
+//                            warps load each chunk's raw activation rows (one
+//                            3-D TMA box per 8-row tile) into a separate ring
+//                            of activation slots and turn them into the
+//                            chunk's tensor-core fragments, the per-group
+//                            activation sums XS (the "b*XS" term of the
+//                            dequant-after-dot form, vmlx-swift PR #565,
+//                            LaneQMM commit) and the range factors. Eight
+//                            consumer warps unpack the codes in registers and
+//                            contract them on tensor cores, reading each code
+//                            byte once for all M rows (same page,
+//                            qwen_qmv_rows_full commit: weights read once per
+//                            k-block for all rows).
 //   2. qmm_splitk_reduce_kernel (splits > 1 only) -- sums the fp32 slice
 //                            partials in slice order (same page, "JANGH split-K
 //                            verify tile" commit: FP32 partials, then a sum).
@@ -113,9 +115,9 @@ struct ReduceParams {
 
 // ---------------------------------------------------------------------------
 // Work enumeration shared by every warp role. The flattened (bank, split, row)
-// space is cut evenly over the CTAs; a CTA's range is cut at (bank, split)
-// boundaries and then into balanced row blocks of <= kTN rows; every row block
-// walks the chunks of its K slice. One item = one chunk of one row block (for
+// space is cut evenly, in whole 16-row slabs, over the CTAs; a CTA's range is
+// cut at (bank, split) boundaries and then into row blocks of kTN rows (the
+// last one shorter); every row block walks the chunks of its K slice. One item = one chunk of one row block (for
 // the fused gate/up projection, each row block is walked for bank 0 (gate) and
 // then for bank 1 (up)).
 // ---------------------------------------------------------------------------
