@@ -56,8 +56,7 @@ int chunks_of(const qmm_desc* d) {
 // Largest K-slice count a plan for d may use (the automatic choice never exceeds it).
 int splits_cap(const qmm_desc* d) {
     if (d->splits > 0) return d->splits;
-    int c = chunks_of(d) / 2;
-    if (c < 1) c = 1;
+    int c = chunks_of(d);
     if (c > 8) c = 8;
     return c;
 }

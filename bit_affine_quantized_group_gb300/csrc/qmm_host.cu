@@ -31,8 +31,9 @@ int chunk_count(int64_t K, int group) { return static_cast<int>((K / group + kGP
 // plus about 2 us of restart, and slicing adds about 3.7 us for the partial
 // sums and their reduce. The work is cut evenly over (bank, slice, row) space,
 // so when the CTA count is not a multiple of the bank-slice segments some CTA
-// ranges straddle two segments and pay one more row block. Slices keep at
-// least 2 chunks.
+// ranges straddle two segments and pay one more row block. A slice may be a
+// single chunk (tiny projections such as K = 2048 in groups of 64 gain from
+// four one-chunk slices).
 int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, int num_sms, int cap) {
     const int C = chunk_count(K, group);
     const double chunk_us = kTN * (chunk_row_bytes(bits, group) + 4.0 * kGPC) / 28e3;
@@ -41,7 +42,7 @@ int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, i
     int best = 1;
     double best_cost = 0.0;
     for (int s = 1; s <= cap; ++s) {
-        if (s > 1 && C / s < 2) break;
+        if (s > C) break;
         const int64_t rows_total = banks * s * N;
         int64_t ctas = (rows_total + kSlab - 1) / kSlab;
         if (ctas > num_sms) ctas = num_sms;

@@ -104,8 +104,7 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
         }
         // 3. K slices: the automatic choice, lowered until the partial sums fit;
         //    then the consumer layout, as qmm_forward chooses it.
-        int cap = C / 2;
-        if (cap < 1) cap = 1;
+        int cap = C;
         if (cap > 8) cap = 8;
         splits = auto_split_count(K, N, bits, group, 1, s.num_sms, cap);
         const size_t per_split = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);

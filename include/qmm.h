@@ -123,7 +123,7 @@ int qmm_validate_desc(const qmm_desc* d);
  * Device workspace a plan for `d` needs (bytes; 0 if d is invalid): a
  * 256-byte error word plus split-K partials for max_banks * splits * max_M * N
  * floats (splits = 0 is sized for the largest automatic choice,
- * min(8, chunks / 2) with chunks = ceil(K / group / 8)). Lets the caller
+ * min(8, chunks) with chunks = ceil(K / group / 8)). Lets the caller
  * (e.g. PyTorch's allocator) own it.
  */
 size_t qmm_workspace_bytes(const qmm_desc* d);
