@@ -2,10 +2,11 @@
 fused gate/up projection.
 
 The small-shape tests give every CTA only a few 16-row slabs and mostly
-partial chunks. Here N = 17408 puts about 115 weight rows on each of the 152
-CTAs of a GB300 (every slab of a 128-row block live) and K is a whole number
-of 8-group chunks, so every width and group size runs the kernel's full-chunk,
-full-block path that the named workloads use, against the oracle:
+partial chunks. Here N = 17408 puts 112 or 128 weight rows (7 or 8 whole
+slabs) on each of the 152 CTAs of a GB300, so the 8-row kernel takes its wide
+consumer layout wherever the format leaves it four weight stages, and K is a
+whole number of 8-group chunks: every width and group size runs the kernel's
+full-chunk, full-block path that the named workloads use, against the oracle:
 
 * all 12 formats (2/3/4/5/6/8-bit codes, groups of 32 and 64), 1, 9 and 16
   rows, one and two K slices, both output types;

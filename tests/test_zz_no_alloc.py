@@ -78,6 +78,7 @@ CASES = [
     (4, 2048, 2048, 4, 64, "f32"),
     (9, 5120, 1000, 6, 32, "bf16"),
     (16, 1024, 520, 8, 32, "bf16"),
+    (8, 5120, 17408, 4, 32, "bf16"),     # 112-128 rows a CTA: the wide consumer layout
     (8, 17408, 5120, 4, 64, "bf16"),     # long K: the automatic choice slices K, partials in the static array
     (16, 16384, 20480, 4, 64, "bf16"),   # partials of the automatic choice exceed the array: fewer slices
 ]
