@@ -23,8 +23,8 @@ struct qmm_plan {
     int splits;
     int C;
     int G;
-    int stages[3];       // index 0: M <= 8 (MB = 8, narrow), 1: M > 8 (MB = 16), 2: M <= 8 wide (0: not usable)
-    int smem[3];
+    int stages[6];       // index 3 * (M > 8) + layout (kNarrow, kWide, kPair); 0: not usable
+    int smem[6];
     uint8_t* ws;
     size_t ws_bytes;
     bool owns_ws;
@@ -39,13 +39,14 @@ namespace {
 constexpr size_t kErrBytes = 256;
 
 // Index into the plan's stages/smem of the main kernel that a call of M rows
-// over rows_total flattened rows (banks x slices x N) launches.
-int layout_index(const struct qmm_plan* p, int M, int64_t rows_total) {
-    if (M > 8) return 1;
-    if (p->stages[2] == 0) return 0;
+// over rows_total flattened rows (banks x slices x N) launches; `single`: one
+// projection.
+int layout_index(const struct qmm_plan* p, int M, int64_t rows_total, bool single) {
+    const int base = M > 8 ? 3 : 0;
     int64_t ctas = (rows_total + kSlab - 1) / kSlab;
     if (ctas > p->num_sms) ctas = p->num_sms;
-    return wide_layout(p->d.bits, p->d.group, 8, rows_total, ctas, p->optin) ? 2 : 0;
+    const int lay = consumer_layout(p->d.bits, p->d.group, M > 8 ? 16 : 8, rows_total, ctas, single, p->optin);
+    return p->stages[base + lay] != 0 ? base + lay : base + kNarrow;
 }
 
 int chunks_of(const qmm_desc* d) {
@@ -159,23 +160,23 @@ int qmm_plan(qmm_plan_t** plan, const qmm_desc* d, void* workspace, size_t ws_by
     if (p->splits > splits_cap(d)) p->splits = splits_cap(d);
 
     p->optin = optin;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 6; ++i) {
         p->stages[i] = 0;
         p->smem[i] = 0;
     }
-    for (int i = 0; i < 3; ++i) {
-        const int mb = i == 1 ? 16 : 8;
-        const bool wide = i == 2;
+    for (int i = 0; i < 6; ++i) {
+        const int mb = i >= 3 ? 16 : 8;
+        const int lay = i % 3;
         if (mb == 16 && d->max_M <= 8) continue;
-        const int st = stages_for(d->bits, d->group, mb, wide, optin);
+        const int st = stages_for(d->bits, d->group, mb, lay, optin);
         if (st < 2) {
-            if (wide) continue;   // the narrow layout serves every call
+            if (lay != kNarrow) continue;   // the narrow layout serves every call
             delete p;
             return QMM_ERR_UNSUPPORTED;
         }
         p->stages[i] = st;
-        p->smem[i] = main_smem_bytes(d->bits, d->group, mb, wide);
-        if (configure_format(d->bits, d->group, mb, wide, p->smem[i]) != cudaSuccess) {
+        p->smem[i] = main_smem_bytes(d->bits, d->group, mb, lay);
+        if (configure_format(d->bits, d->group, mb, lay, p->smem[i]) != cudaSuccess) {
             delete p;
             return QMM_ERR_CUDA;
         }
@@ -210,11 +211,13 @@ int qmm_plan_get_info(const qmm_plan_t* p, qmm_plan_info* info) {
     if (p == nullptr || info == nullptr) return QMM_ERR_INVALID_ARG;
     info->splits = p->splits;
     info->chunks = p->C;
-    const int l8 = layout_index(p, 1, static_cast<int64_t>(p->splits) * p->d.N);
+    const int64_t rows = static_cast<int64_t>(p->splits) * p->d.N;
+    const int l8 = layout_index(p, 1, rows, true);
+    const int l16 = p->d.max_M > 8 ? layout_index(p, 16, rows, true) : 3;
     info->stages[0] = p->stages[l8];
-    info->stages[1] = p->stages[1];
+    info->stages[1] = p->stages[l16];
     info->smem_bytes[0] = p->smem[l8];
-    info->smem_bytes[1] = p->smem[1];
+    info->smem_bytes[1] = p->smem[l16];
     info->num_sms = p->num_sms;
     info->device = p->device;
     info->workspace_bytes = static_cast<int64_t>(p->ws_bytes);
@@ -258,7 +261,7 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
     if (M == 0) return QMM_OK;
 
     const int64_t rows_total = static_cast<int64_t>(swiglu ? 1 : n_banks) * p->splits * N;
-    const int mi = layout_index(p, M, rows_total);
+    const int mi = layout_index(p, M, rows_total, !swiglu && n_banks == 1);
     if (p->stages[mi] == 0) return QMM_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     struct qmm_plan* mp_plan = const_cast<struct qmm_plan*>(p);   // the tensor-map caches are plan-owned scratch
@@ -284,8 +287,8 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
     int64_t ctas = (h.rows_total + kSlab - 1) / kSlab;
     if (ctas > p->num_sms) ctas = p->num_sms;
     LaunchCfg L;
-    L.mb = mi == 1 ? 16 : 8;
-    L.wide = mi == 2;
+    L.mb = mi >= 3 ? 16 : 8;
+    L.lay = mi % 3;
     L.ctas = static_cast<int>(ctas);
     L.smem = p->smem[mi];
     L.stream = st;

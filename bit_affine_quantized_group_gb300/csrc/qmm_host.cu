@@ -7,20 +7,27 @@
 
 namespace qmmk {
 
-int stages_for(int bits, int group, int mb, bool wide, int optin) {
-    if (wide && mb != 8) return 0;
-    const int st = stage_count(bits, group, mb, wide);
-    return (st >= 2 && main_smem_bytes(bits, group, mb, wide) <= optin) ? st : 0;
+int stages_for(int bits, int group, int mb, int lay, int optin) {
+    if (lay == kWide && mb != 8) return 0;
+    const int st = stage_count(bits, group, mb, lay);
+    return (st >= 2 && main_smem_bytes(bits, group, mb, lay) <= optin) ? st : 0;
 }
 
-// A wide consumer warp owns two slabs of each row block: with CTA row ranges of
-// fewer than 96 rows some wide warps would idle while others carry two slabs,
-// and with fewer than four weight stages each parity would wait for its own
-// refills; the narrow layout (every warp on every item) is then faster.
-bool wide_layout(int bits, int group, int mb, int64_t rows_total, int64_t ctas, int optin) {
-    if (mb != 8 || ctas < 1) return false;
-    if (stages_for(bits, group, 8, true, optin) < 4) return false;
-    return rows_total / ctas >= 96;
+// The pair layout keeps two items in flight with one slab a warp, but covers
+// only 64 rows an item: it serves calls whose longest CTA range has at most
+// four slabs, where the narrow layout would put one item at a time on at most
+// four warps. A wide consumer warp owns two slabs of each row block: with CTA
+// row ranges of fewer than 96 rows some wide warps would idle while others
+// carry two slabs, and with fewer than four weight stages each parity would
+// wait for its own refills; the narrow layout (every warp on every item) is
+// then faster.
+int consumer_layout(int bits, int group, int mb, int64_t rows_total, int64_t ctas, bool single, int optin) {
+    if (ctas < 1) return kNarrow;
+    const int64_t slabs = (rows_total + kSlab - 1) / kSlab;
+    const int64_t longest = (slabs + ctas - 1) / ctas * kSlab;
+    if (single && longest <= consumer_rows(kPair) && stages_for(bits, group, mb, kPair, optin) >= 2) return kPair;
+    if (mb == 8 && stages_for(bits, group, 8, kWide, optin) >= 4 && rows_total / ctas >= 96) return kWide;
+    return kNarrow;
 }
 
 int chunk_count(int64_t K, int group) { return static_cast<int>((K / group + kGPC - 1) / kGPC); }
@@ -32,8 +39,7 @@ int chunk_count(int64_t K, int group) { return static_cast<int>((K / group + kGP
 // sums and their reduce. The work is cut evenly over (bank, slice, row) space,
 // so when the CTA count is not a multiple of the bank-slice segments some CTA
 // ranges straddle two segments and pay one more row block. A slice may be a
-// single chunk (tiny projections such as K = 2048 in groups of 64 gain from
-// four one-chunk slices).
+// single chunk.
 int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, int num_sms, int cap) {
     const int C = chunk_count(K, group);
     const double chunk_us = kTN * (chunk_row_bytes(bits, group) + 4.0 * kGPC) / 28e3;
@@ -50,7 +56,12 @@ int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, i
         int64_t blocks = (rows_per_cta + kTN - 1) / kTN;
         if (ctas % (banks * s) != 0) ++blocks;
         const int per_slice = (C + s - 1) / s;
-        const double cost = blocks * (per_slice * chunk_us + row_block_us) + (s > 1 ? split_us : 0.0);
+        // CTA ranges of at most four slabs take the pair layout (two items in
+        // flight), measured 10-22 % faster per chunk than one item at a time
+        const int64_t slabs = (rows_total + kSlab - 1) / kSlab;
+        const bool pair = banks == 1 && (slabs + ctas - 1) / ctas * kSlab <= consumer_rows(kPair);
+        const double cost = blocks * (per_slice * chunk_us * (pair ? 0.8 : 1.0) + row_block_us) +
+                            (s > 1 ? split_us : 0.0);
         if (s == 1 || cost < best_cost) {
             best = s;
             best_cost = cost;
@@ -59,14 +70,14 @@ int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, i
     return best;
 }
 
-cudaError_t configure_format(int bits, int group, int mb, bool wide, int smem_bytes) {
+cudaError_t configure_format(int bits, int group, int mb, int lay, int smem_bytes) {
     switch (bits) {
-        case 2: return configure_kernels<2>(group, mb, wide, smem_bytes);
-        case 3: return configure_kernels<3>(group, mb, wide, smem_bytes);
-        case 4: return configure_kernels<4>(group, mb, wide, smem_bytes);
-        case 5: return configure_kernels<5>(group, mb, wide, smem_bytes);
-        case 6: return configure_kernels<6>(group, mb, wide, smem_bytes);
-        case 8: return configure_kernels<8>(group, mb, wide, smem_bytes);
+        case 2: return configure_kernels<2>(group, mb, lay, smem_bytes);
+        case 3: return configure_kernels<3>(group, mb, lay, smem_bytes);
+        case 4: return configure_kernels<4>(group, mb, lay, smem_bytes);
+        case 5: return configure_kernels<5>(group, mb, lay, smem_bytes);
+        case 6: return configure_kernels<6>(group, mb, lay, smem_bytes);
+        case 8: return configure_kernels<8>(group, mb, lay, smem_bytes);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -13,14 +13,13 @@ namespace qmmk {
 
 // The format's pipeline depth (stage_count, fixed at compile time) for a row
 // tile and consumer layout when its main-kernel shared memory fits `optin`
-// bytes; 0 otherwise.
-int stages_for(int bits, int group, int mb, bool wide, int optin);
+// bytes; 0 otherwise (also for the wide layout of the 16-row tile).
+int stages_for(int bits, int group, int mb, int lay, int optin);
 
-// Consumer layout of a call's main kernel: wide (two slabs a warp, two
-// parities; 8-row kernel only) when the CTAs' row ranges fill most of a
-// 128-row block and the wide layout keeps at least four weight stages;
-// narrow otherwise.
-bool wide_layout(int bits, int group, int mb, int64_t rows_total, int64_t ctas, int optin);
+// Consumer layout (kNarrow, kWide, kPair) of a call's main kernel over
+// rows_total flattened rows on `ctas` CTAs; `single`: one projection (the
+// pair layout is compiled for those only).
+int consumer_layout(int bits, int group, int mb, int64_t rows_total, int64_t ctas, bool single, int optin);
 
 // 8-group chunks along K.
 int chunk_count(int64_t K, int group);
@@ -31,7 +30,7 @@ int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, i
 
 // Set the main kernels' dynamic shared-memory limit for one format, row tile
 // and consumer layout.
-cudaError_t configure_format(int bits, int group, int mb, bool wide, int smem_bytes);
+cudaError_t configure_format(int bits, int group, int mb, int lay, int smem_bytes);
 
 // Launch the main kernel of one format (exactly one of the parameter blocks is non-null).
 cudaError_t launch_format(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,

@@ -7,19 +7,28 @@
 namespace qmmk {
 
 namespace {
-template <int BITS, int GROUP, int MB, bool WIDE>
-cudaError_t configure_one(int smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 1, WIDE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, 2, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, kMaxBanks, WIDE>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+template <int BITS, int GROUP, int MB, int CAP, int LAY>
+cudaError_t configure_cap(int smem_bytes) {
+    return cudaFuncSetAttribute(qmm_main_kernel<BITS, GROUP, MB, CAP, LAY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes);
 }
 
-template <int BITS, int GROUP, int MB, int CAP, bool WIDE>
+// The pair layout is compiled for single projections only; banked and fused
+// calls use the narrow or wide layout.
+template <int BITS, int GROUP, int MB, int LAY>
+cudaError_t configure_one(int smem_bytes) {
+    cudaError_t e = configure_cap<BITS, GROUP, MB, 1, LAY>(smem_bytes);
+    if constexpr (LAY == kPair) {
+        return e;
+    } else {
+        if (e != cudaSuccess) return e;
+        e = configure_cap<BITS, GROUP, MB, 2, LAY>(smem_bytes);
+        if (e != cudaSuccess) return e;
+        return configure_cap<BITS, GROUP, MB, kMaxBanks, LAY>(smem_bytes);
+    }
+}
+
+template <int BITS, int GROUP, int MB, int CAP, int LAY>
 cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     // The main kernel is a programmatic dependent of whatever precedes it on the
     // stream: it is scheduled as soon as that work allows (its CTAs take SMs as
@@ -36,38 +45,54 @@ cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     cfg.stream = L.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP, WIDE>, mp);
+    return cudaLaunchKernelEx(&cfg, qmm_main_kernel<BITS, GROUP, MB, CAP, LAY>, mp);
 }
 
-template <int BITS, int GROUP, int MB, bool WIDE>
+template <int BITS, int GROUP, int MB, int LAY>
 cudaError_t launch_cap(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked,
                        const MainParams<2>* fused) {
-    if (single) return launch_one<BITS, GROUP, MB, 1, WIDE>(L, *single);
-    if (fused) return launch_one<BITS, GROUP, MB, 2, WIDE>(L, *fused);
-    return launch_one<BITS, GROUP, MB, kMaxBanks, WIDE>(L, *banked);
+    if (single) return launch_one<BITS, GROUP, MB, 1, LAY>(L, *single);
+    if constexpr (LAY == kPair) {
+        return cudaErrorInvalidValue;
+    } else {
+        if (fused) return launch_one<BITS, GROUP, MB, 2, LAY>(L, *fused);
+        return launch_one<BITS, GROUP, MB, kMaxBanks, LAY>(L, *banked);
+    }
 }
 
 template <int BITS, int GROUP>
-cudaError_t configure_group(int mb, bool wide, int smem_bytes) {
-    if (mb == 16) return wide ? cudaErrorInvalidValue : configure_one<BITS, GROUP, 16, false>(smem_bytes);
-    return wide ? configure_one<BITS, GROUP, 8, true>(smem_bytes) : configure_one<BITS, GROUP, 8, false>(smem_bytes);
+cudaError_t configure_group(int mb, int lay, int smem_bytes) {
+    if (mb == 16) {
+        if (lay == kNarrow) return configure_one<BITS, GROUP, 16, kNarrow>(smem_bytes);
+        if (lay == kPair) return configure_one<BITS, GROUP, 16, kPair>(smem_bytes);
+        return cudaErrorInvalidValue;
+    }
+    if (lay == kNarrow) return configure_one<BITS, GROUP, 8, kNarrow>(smem_bytes);
+    if (lay == kWide) return configure_one<BITS, GROUP, 8, kWide>(smem_bytes);
+    if (lay == kPair) return configure_one<BITS, GROUP, 8, kPair>(smem_bytes);
+    return cudaErrorInvalidValue;
 }
 
 template <int BITS, int GROUP>
 cudaError_t launch_group(const LaunchCfg& L, const MainParams<1>* single, const MainParams<kMaxBanks>* banked,
                          const MainParams<2>* fused) {
-    if (L.mb == 16)
-        return L.wide ? cudaErrorInvalidValue : launch_cap<BITS, GROUP, 16, false>(L, single, banked, fused);
-    return L.wide ? launch_cap<BITS, GROUP, 8, true>(L, single, banked, fused)
-                  : launch_cap<BITS, GROUP, 8, false>(L, single, banked, fused);
+    if (L.mb == 16) {
+        if (L.lay == kNarrow) return launch_cap<BITS, GROUP, 16, kNarrow>(L, single, banked, fused);
+        if (L.lay == kPair) return launch_cap<BITS, GROUP, 16, kPair>(L, single, banked, fused);
+        return cudaErrorInvalidValue;
+    }
+    if (L.lay == kNarrow) return launch_cap<BITS, GROUP, 8, kNarrow>(L, single, banked, fused);
+    if (L.lay == kWide) return launch_cap<BITS, GROUP, 8, kWide>(L, single, banked, fused);
+    if (L.lay == kPair) return launch_cap<BITS, GROUP, 8, kPair>(L, single, banked, fused);
+    return cudaErrorInvalidValue;
 }
 }  // namespace
 
 template <>
-cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, bool wide, int smem_bytes) {
+cudaError_t configure_kernels<QMM_INST_BITS>(int group, int mb, int lay, int smem_bytes) {
     constexpr int B = QMM_INST_BITS;
-    if (group == 32) return configure_group<B, 32>(mb, wide, smem_bytes);
-    if (group == 64) return configure_group<B, 64>(mb, wide, smem_bytes);
+    if (group == 32) return configure_group<B, 32>(mb, lay, smem_bytes);
+    if (group == 64) return configure_group<B, 64>(mb, lay, smem_bytes);
     return cudaErrorInvalidValue;
 }
 

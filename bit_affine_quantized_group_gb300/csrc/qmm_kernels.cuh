@@ -220,13 +220,13 @@ __device__ __forceinline__ int wtile_off(int r, int b) {
 // ---------------------------------------------------------------------------
 // The main kernel.
 // ---------------------------------------------------------------------------
-template <int BITS, int GROUP, int MB, int CAP, bool WIDE>
+template <int BITS, int GROUP, int MB, int CAP, int LAY>
 __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
     constexpr int NT = n8_tiles(MB);
     constexpr int NSW = staging_warps(MB);
-    static_assert(MB == 8 || !WIDE, "the wide consumer layout is for the 8-row kernel");
+    static_assert(MB == 8 || LAY != kWide, "the wide consumer layout is for the 8-row kernel");
     constexpr int NCW = consumer_warps();
-    constexpr int CPAR = consumer_parities(WIDE);
+    constexpr int CPAR = consumer_parities(LAY);
     constexpr int WPPC = NCW / CPAR;             // consumer warps of one parity
     constexpr int VB = vblocks_per_group(GROUP);
     constexpr int VPC = vblocks_per_chunk(GROUP);
@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
     // array so every access below stays a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    constexpr int S = stage_count(BITS, GROUP, MB, WIDE);     // weight stages
-    constexpr int F = act_slots(BITS, GROUP, MB, WIDE);       // activation slots
+    constexpr int S = stage_count(BITS, GROUP, MB, LAY);     // weight stages
+    constexpr int F = act_slots(BITS, GROUP, MB, LAY);       // activation slots
     static_assert(S >= 2 && F >= 2 && S % CPAR == 0 && F % CPAR == 0, "pipeline depth");
     uint8_t* aring = smem + S * WSB;                                        // activation slots
     uint64_t* wfull = reinterpret_cast<uint64_t*>(aring + F * ASB);        // weights, scales, biases landed
@@ -325,6 +325,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                     (wi.n0 >= 0 && wi.rows >= 1 && wi.rows <= kTN && wi.n0 + wi.rows <= p.N && wi.c0 >= 0 &&
                      wi.c1 <= p.C && ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & 3) == 0);
                 if (!sb_ok && lane == 0) record_bad_copy(p.err, bp.s, static_cast<uint64_t>(wi.rows), 4u);
+                // the host gives a layout only row blocks it covers; a longer one
+                // would leave rows unwritten, so it is recorded
+                if (wi.rows > consumer_rows(LAY) && lane == 0)
+                    record_bad_copy(p.err, bp.w, static_cast<uint64_t>(wi.rows), 6u);
             }
             // After a timed-out wait the error is recorded and no further waits are
             // made; the loop still runs to the end so that every warp finishes.
@@ -647,8 +651,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     // chunks in the stage slots of parity cp (all slots when CPAR == 1). The
     // slabs of a warp share its activation fragment loads and give it SPW
     // independent MMA chains.
-    constexpr int SPW = consumer_slabs(WIDE);
-    constexpr int WPP = kSlabs / SPW;            // consumer warps per parity
+    constexpr int SPW = consumer_slabs(LAY);
+    constexpr int WPP = NCW / CPAR;              // consumer warps per parity
     const int w = warp % WPP;
     const int cp = warp / WPP;
     const int r0 = kSlab * SPW * w + g;          // first slab's row; slab s: r0 + 16 s
@@ -1023,7 +1027,7 @@ __global__ void __launch_bounds__(256) qmm_unpack_kernel(const uint32_t* __restr
 // ---------------------------------------------------------------------------
 struct LaunchCfg {
     int mb;            // 8 or 16
-    bool wide;         // consumer layout (8-row kernel only)
+    int lay;           // consumer layout (kNarrow, kWide: 8-row kernel only, kPair)
     int ctas;
     int smem;
     cudaStream_t stream;
@@ -1032,7 +1036,7 @@ struct LaunchCfg {
 // Set the dynamic shared-memory limit of one format's main kernels for one row
 // tile and consumer layout (every bank capacity).
 template <int BITS>
-cudaError_t configure_kernels(int group, int mb, bool wide, int smem_bytes);
+cudaError_t configure_kernels(int group, int mb, int lay, int smem_bytes);
 
 // Weight-box width for a format (host side, for encoding tensor maps).
 inline int weight_box_width(int bits, int group) { return wbox_width(bits, group); }

@@ -51,17 +51,29 @@ QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
 // tile owning the activation slots s with s % staging_per_tile == p.
 QMM_HD constexpr int staging_per_tile(int mb) { return mb == 8 ? 6 : 2; }
 QMM_HD constexpr int staging_warps(int mb) { return staging_per_tile(mb) * n8_tiles(mb); }
-// Consumer warps, in one of two layouts, 8 warps either way (with the staging
+// Consumer warps, in one of three layouts, 8 warps each (with the staging
 // warps and the producer at most four warps share a scheduler: 128 registers a
 // thread):
-//   * narrow: one 16-row slab a warp, every work item;
+//   * narrow: one 16-row slab a warp, every work item (128 rows an item);
 //   * wide (8-row kernel only): two slabs a warp (two independent MMA chains
 //     sharing the activation fragment loads) in two parities, parity p taking
-//     the items in the stage slots of parity p. It pays when a CTA's row blocks
-//     fill most of the 8 slabs and the pipeline keeps several stages per parity.
-QMM_HD constexpr int consumer_slabs(bool wide) { return wide ? 2 : 1; }
-QMM_HD constexpr int consumer_parities(bool wide) { return wide ? 2 : 1; }
+//     the items in the stage slots of parity p (128 rows an item). It pays when
+//     a CTA's row blocks fill most of the 8 slabs and the pipeline keeps
+//     several stages per parity;
+//   * pair: one slab a warp in two parities (64 rows an item), two items in
+//     flight for CTAs of at most four slabs.
+// Every layout sums a block's even- and odd-index items apart and adds the two
+// at the end, so they all give the same bits.
+constexpr int kNarrow = 0;
+constexpr int kWide = 1;
+constexpr int kPair = 2;
+QMM_HD constexpr int consumer_slabs(int lay) { return lay == kWide ? 2 : 1; }
+QMM_HD constexpr int consumer_parities(int lay) { return lay == kNarrow ? 1 : 2; }
 QMM_HD constexpr int consumer_warps() { return kSlabs; }
+// Rows of a row block the consumers cover (a CTA's blocks must not be longer).
+QMM_HD constexpr int consumer_rows(int lay) {
+    return kSlab * consumer_slabs(lay) * consumer_warps() / consumer_parities(lay);
+}
 QMM_HD constexpr int main_threads(int mb) { return (consumer_warps() + staging_warps(mb) + 1) * 32; }
 
 // k32 blocks per scale group and per chunk.
@@ -111,46 +123,48 @@ QMM_HD constexpr int wstage_bytes(int bits, int group) {
 QMM_HD constexpr int aslot_bytes(int group, int mb) { return round_up(xraw_bytes(group, mb) + xstaged_bytes(group, mb), 1024); }
 
 // Scratch for adding the second consumer parity's partial sums at the end of
-// a row block (wide layout): [slab][tile][4][32 lanes] floats.
-QMM_HD constexpr int combine_bytes(int mb, bool wide) { return wide ? kSlabs * n8_tiles(mb) * 4 * 32 * 4 : 0; }
+// a row block (wide and pair layouts): [slab][tile][4][32 lanes] floats.
+QMM_HD constexpr int combine_bytes(int mb, int lay) {
+    return consumer_parities(lay) > 1 ? consumer_rows(lay) / kSlab * n8_tiles(mb) * 4 * 32 * 4 : 0;
+}
 
 // Dynamic shared memory of the main kernel with S weight stages and F
 // activation slots: the stages, the slots, two mbarriers per weight stage
 // (landed, consumed), per activation slot one per tile (raw landed) and two
 // more (staged, consumed), and the combine scratch. 1024 bytes of slack let the kernel align
 // its rings to 1024.
-QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, bool wide, int S, int F) {
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int lay, int S, int F) {
     return 1024 + S * wstage_bytes(bits, group) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
-           combine_bytes(mb, wide);
+           combine_bytes(mb, lay);
 }
 // The most weight stages (<= kMaxStages) that fit kSmemOptin next to F
 // activation slots, a multiple of the consumer parities (each parity owns the
 // stages of its parity); 0 if fewer than two fit.
-QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, bool wide, int F) {
-    return (main_smem_bytes(bits, group, mb, wide, 8, F) <= kSmemOptin   ? 8
-          : main_smem_bytes(bits, group, mb, wide, 7, F) <= kSmemOptin ? 7
-          : main_smem_bytes(bits, group, mb, wide, 6, F) <= kSmemOptin ? 6
-          : main_smem_bytes(bits, group, mb, wide, 5, F) <= kSmemOptin ? 5
-          : main_smem_bytes(bits, group, mb, wide, 4, F) <= kSmemOptin ? 4
-          : main_smem_bytes(bits, group, mb, wide, 3, F) <= kSmemOptin ? 3
-          : main_smem_bytes(bits, group, mb, wide, 2, F) <= kSmemOptin ? 2
+QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, int lay, int F) {
+    return (main_smem_bytes(bits, group, mb, lay, 8, F) <= kSmemOptin   ? 8
+          : main_smem_bytes(bits, group, mb, lay, 7, F) <= kSmemOptin ? 7
+          : main_smem_bytes(bits, group, mb, lay, 6, F) <= kSmemOptin ? 6
+          : main_smem_bytes(bits, group, mb, lay, 5, F) <= kSmemOptin ? 5
+          : main_smem_bytes(bits, group, mb, lay, 4, F) <= kSmemOptin ? 4
+          : main_smem_bytes(bits, group, mb, lay, 3, F) <= kSmemOptin ? 3
+          : main_smem_bytes(bits, group, mb, lay, 2, F) <= kSmemOptin ? 2
                                                                         : 0) /
-           consumer_parities(wide) * consumer_parities(wide);
+           consumer_parities(lay) * consumer_parities(lay);
 }
 // Activation slots: a multiple of the consumer parities, and either at most
 // the staging warps per tile or a multiple of them (each warp owns whole
 // slots); the larger choice when it still leaves four weight stages.
-QMM_HD constexpr int act_slots(int bits, int group, int mb, bool wide) {
-    return mb == 8 ? (weight_stages_for(bits, group, mb, wide, 6) >= 4   ? 6
-                      : weight_stages_for(bits, group, mb, wide, 4) >= 4 ? 4
+QMM_HD constexpr int act_slots(int bits, int group, int mb, int lay) {
+    return mb == 8 ? (weight_stages_for(bits, group, mb, lay, 6) >= 4   ? 6
+                      : weight_stages_for(bits, group, mb, lay, 4) >= 4 ? 4
                                                                          : 2)
-                   : (weight_stages_for(bits, group, mb, wide, 4) >= 4 ? 4 : 2);
+                   : (weight_stages_for(bits, group, mb, lay, 4) >= 4 ? 4 : 2);
 }
-QMM_HD constexpr int stage_count(int bits, int group, int mb, bool wide) {
-    return weight_stages_for(bits, group, mb, wide, act_slots(bits, group, mb, wide));
+QMM_HD constexpr int stage_count(int bits, int group, int mb, int lay) {
+    return weight_stages_for(bits, group, mb, lay, act_slots(bits, group, mb, lay));
 }
-QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, bool wide) {
-    return main_smem_bytes(bits, group, mb, wide, stage_count(bits, group, mb, wide), act_slots(bits, group, mb, wide));
+QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int lay) {
+    return main_smem_bytes(bits, group, mb, lay, stage_count(bits, group, mb, lay), act_slots(bits, group, mb, lay));
 }
 
 }  // namespace qmmk

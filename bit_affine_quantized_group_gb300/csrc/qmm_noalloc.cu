@@ -45,7 +45,7 @@ struct DeviceSetup {
     uint8_t* scratch;         // device address of g_noalloc_scratch on this device
     int num_sms;
     int optin;
-    uint64_t configured;      // bit (bits_index * 6 + group_index * 3 + layout): kernel attributes set
+    uint64_t configured;      // bit (bits_index * 8 + group_index * 4 + 3 * (16-row tile) + layout): attributes set
 };
 
 DeviceSetup g_dev[kMaxDevices];
@@ -83,7 +83,7 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QMM_ERR_CUDA;
     DeviceSetup ds;
     int stages = 0;
-    bool wide = false;
+    int lay = kNarrow;
     int splits = 1;
     const int C = chunk_count(K, group);
     {
@@ -112,13 +112,13 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
         const int64_t rows = static_cast<int64_t>(splits) * N;
         int64_t ctas = (rows + kSlab - 1) / kSlab;
         if (ctas > s.num_sms) ctas = s.num_sms;
-        wide = wide_layout(bits, group, mb, rows, ctas, s.optin);
-        stages = stages_for(bits, group, mb, wide, s.optin);
+        lay = consumer_layout(bits, group, mb, rows, ctas, true, s.optin);
+        stages = stages_for(bits, group, mb, lay, s.optin);
         if (stages < 2) return QMM_ERR_UNSUPPORTED;
-        const int layout = mb == 16 ? 1 : (wide ? 2 : 0);
-        const uint64_t cfg_bit = 1ull << (bits_index(bits) * 6 + (group == 64 ? 3 : 0) + layout);
+        const int layout = (mb == 16 ? 3 : 0) + lay;
+        const uint64_t cfg_bit = 1ull << (bits_index(bits) * 8 + (group == 64 ? 4 : 0) + layout);
         if (!(s.configured & cfg_bit)) {
-            if (configure_format(bits, group, mb, wide, main_smem_bytes(bits, group, mb, wide)) != cudaSuccess)
+            if (configure_format(bits, group, mb, lay, main_smem_bytes(bits, group, mb, lay)) != cudaSuccess)
                 return QMM_ERR_CUDA;
             s.configured |= cfg_bit;
         }
@@ -160,9 +160,9 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     if (ctas > ds.num_sms) ctas = ds.num_sms;
     LaunchCfg L;
     L.mb = mb;
-    L.wide = wide;
+    L.lay = lay;
     L.ctas = static_cast<int>(ctas);
-    L.smem = main_smem_bytes(bits, group, mb, wide);
+    L.smem = main_smem_bytes(bits, group, mb, lay);
     L.stream = st;
     if (launch_format(bits, group, L, &mp, nullptr, nullptr) != cudaSuccess) return QMM_ERR_CUDA;
     if (splits > 1) {

@@ -182,36 +182,39 @@ def test_row_independence(q, oracle_mod, bits, group, splits):
 
 @pytest.mark.parametrize("bits", [4, 5, 8])
 def test_consumer_layouts_agree(q, oracle_mod, bits):
-    """The 8-row kernel's two consumer layouts (wide: two slabs a warp in two
-    item parities; narrow: one slab a warp on every item, keeping the even- and
-    odd-item sums apart) add the same terms in the same order. A projection
-    with about 112 rows per CTA takes the wide layout, one with a few rows per
-    CTA the narrow one; on the same weights and x their shared rows must agree
-    bitwise (K spans an even number of 8-group chunks, so each row block's
-    items split the same way), and the narrow result must match the oracle."""
+    """The consumer layouts add the same terms in the same order: every layout
+    sums a row block's even- and odd-index items apart and adds the two. A
+    projection with 112 rows per CTA takes the wide layout at 1-8 rows, one with
+    80 rows per CTA the narrow layout, one with 48 rows per CTA the pair layout
+    (two items in flight); at 9-16 rows the first two are narrow and the third
+    pair. On the same weights and x their shared rows must agree bitwise (K
+    spans an even number of 8-group chunks, so each row block's items split the
+    same way), and the smallest result must match the oracle."""
     import torch
     K, group = 5120, 32
     probe = q.Plan(K, 1024, bits, group, max_M=8, out_dtype="f32", splits=1)
     sms = probe.info()["num_sms"]
     probe.close()
-    N_wide, N_narrow = sms * 112, 1024
-    inp = datagen.gen_qmm(77 + bits, 8, K, N_wide, bits, group)
+    Ns = [sms * 112, sms * 80, sms * 48]
+    inp = datagen.gen_qmm(77 + bits, 16, K, Ns[0], bits, group)
     x, w, s, b = dev_tensors(inp)
     row_bytes = K * bits // 8
     G = K // group
-    w_n = w.view(torch.uint8).view(N_wide, row_bytes)[:N_narrow].contiguous().view(torch.int32)
-    s_n, b_n = s.view(N_wide, G)[:N_narrow].contiguous(), b.view(N_wide, G)[:N_narrow].contiguous()
-    plan_w = q.Plan(K, N_wide, bits, group, max_M=8, out_dtype="f32", splits=1)
-    plan_n = q.Plan(K, N_narrow, bits, group, max_M=8, out_dtype="f32", splits=1)
-    for M in (1, 8):
-        y_w = to_f64(run_forward(plan_w, x, w, s, b, M))
-        y_n = to_f64(run_forward(plan_n, x, w_n, s_n, b_n, M))
-        assert np.array_equal(y_w[:, :N_narrow], y_n), (M, np.abs(y_w[:, :N_narrow] - y_n).max())
-        cols = np.arange(0, N_narrow, 7, dtype=np.int64)
-        y_ref = oracle_mod.qmm_f64_cols(inp.x[:M], inp.words[0], inp.scales[0], inp.biases[0], K, N_wide, bits,
+
+    def prefix(n):
+        return (w.view(torch.uint8).view(Ns[0], row_bytes)[:n].contiguous().view(torch.int32),
+                s.view(Ns[0], G)[:n].contiguous(), b.view(Ns[0], G)[:n].contiguous())
+    plans = [q.Plan(K, n, bits, group, max_M=16, out_dtype="f32", splits=1) for n in Ns]
+    for M in (1, 8, 16):
+        ys = [to_f64(run_forward(pl, x, *prefix(n), M)) for pl, n in zip(plans, Ns)]
+        for i in (1, 2):
+            n = Ns[i]
+            assert np.array_equal(ys[i - 1][:, :n], ys[i]), (M, i, np.abs(ys[i - 1][:, :n] - ys[i]).max())
+        cols = np.arange(0, Ns[2], 11, dtype=np.int64)
+        y_ref = oracle_mod.qmm_f64_cols(inp.x[:M], inp.words[0], inp.scales[0], inp.biases[0], K, Ns[0], bits,
                                         group, cols)
-        check(y_n[:, cols], y_ref, "f32")
-    assert plan_w.error_flags() == 0 and plan_n.error_flags() == 0
+        check(ys[2][:, cols], y_ref, "f32")
+    assert all(pl.error_flags() == 0 for pl in plans)
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
