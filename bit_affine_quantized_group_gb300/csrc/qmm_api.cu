@@ -30,8 +30,9 @@ struct qmm_plan {
     bool owns_ws;
     uint32_t* err;       // device error word (start of the workspace)
     float* partial;
-    // TMA tensor maps already encoded for a given base pointer (weights, scales, biases)
-    std::unordered_map<const void*, CUtensorMap> wmaps, smaps, bmaps;
+    // TMA tensor maps already encoded for a given base pointer (weights, scales,
+    // biases), for row blocks of kTN rows [0] and of the pair layout's rows [1]
+    std::unordered_map<const void*, CUtensorMap> wmaps[2], smaps[2], bmaps[2];
 };
 
 namespace {
@@ -79,15 +80,15 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 // Cached lookup; the cache is cleared when it grows past a few thousand pointers.
 bool tensor_map_for(struct qmm_plan* p, std::unordered_map<const void*, CUtensorMap>& cache, const void* ptr, bool weights,
-                    CUtensorMap* out) {
+                    int rows, CUtensorMap* out) {
     auto it = cache.find(ptr);
     if (it != cache.end()) {
         *out = it->second;
         return true;
     }
     CUtensorMap m;
-    if (!(weights ? encode_weight_map(ptr, p->d.K, p->d.N, p->d.bits, p->d.group, &m)
-                  : encode_sb_map(ptr, p->G, p->d.N, &m)))
+    if (!(weights ? encode_weight_map(ptr, p->d.K, p->d.N, p->d.bits, p->d.group, rows, &m)
+                  : encode_sb_map(ptr, p->G, p->d.N, rows, &m)))
         return false;
     if (cache.size() >= 4096) cache.clear();
     cache.emplace(ptr, m);
@@ -289,6 +290,8 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
     LaunchCfg L;
     L.mb = mi >= 3 ? 16 : 8;
     L.lay = mi % 3;
+    const int rows = consumer_rows(L.lay);           // weight and scale boxes: one row block
+    const int mc = rows == kTN ? 0 : 1;
     L.ctas = static_cast<int>(ctas);
     L.smem = p->smem[mi];
     L.stream = st;
@@ -303,10 +306,10 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
             mp.bank[i].s = scales_f16[i];
             mp.bank[i].b = biases_f16[i];
             mp.bank[i].out = out[i];
-            if (!tensor_map_for(mp_plan, mp_plan->wmaps, packed_w[i], true, &mp.tmw[i])) return false;
+            if (!tensor_map_for(mp_plan, mp_plan->wmaps[mc], packed_w[i], true, rows, &mp.tmw[i])) return false;
             if (h.sb_tma) {
-                if (!tensor_map_for(mp_plan, mp_plan->smaps, scales_f16[i], false, &mp.tms[i])) return false;
-                if (!tensor_map_for(mp_plan, mp_plan->bmaps, biases_f16[i], false, &mp.tmb[i])) return false;
+                if (!tensor_map_for(mp_plan, mp_plan->smaps[mc], scales_f16[i], false, rows, &mp.tms[i])) return false;
+                if (!tensor_map_for(mp_plan, mp_plan->bmaps[mc], biases_f16[i], false, rows, &mp.tmb[i])) return false;
             }
         }
         return true;

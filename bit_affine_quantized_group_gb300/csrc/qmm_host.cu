@@ -112,14 +112,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 }  // namespace
 
-bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group, CUtensorMap* out) {
+bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group, int rows, CUtensorMap* out) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const int W = wbox_width(bits, group);
     const cuuint64_t row_bytes = static_cast<cuuint64_t>(K * bits / 8);
     const cuuint64_t dims[2] = {row_bytes, static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(W), static_cast<cuuint32_t>(kTN)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(W), static_cast<cuuint32_t>(rows)};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapSwizzle sw = W == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                            : (W == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
@@ -128,12 +128,12 @@ bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_sb_map(const void* a, int64_t G, int64_t N, CUtensorMap* out) {
+bool encode_sb_map(const void* a, int64_t G, int64_t N, int rows, CUtensorMap* out) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGPC), static_cast<cuuint32_t>(kTN)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGPC), static_cast<cuuint32_t>(rows)};
     const cuuint32_t estr[2] = {1, 1};
     return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

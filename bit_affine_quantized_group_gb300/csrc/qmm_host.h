@@ -36,10 +36,11 @@ cudaError_t configure_format(int bits, int group, int mb, int lay, int smem_byte
 cudaError_t launch_format(int bits, int group, const LaunchCfg& L, const MainParams<1>* single,
                           const MainParams<kMaxBanks>* banked, const MainParams<2>* fused);
 
-// Packed codes as uint8 [N][K*bits/8], box kTN rows x W bytes with the W-byte swizzle.
-bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group, CUtensorMap* out);
-// Scales or biases as uint16 [N][G], box kTN rows x 8 values, unswizzled.
-bool encode_sb_map(const void* a, int64_t G, int64_t N, CUtensorMap* out);
+// Packed codes as uint8 [N][K*bits/8], box `rows` rows (the consumer layout's
+// block rows) x W bytes with the W-byte swizzle.
+bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group, int rows, CUtensorMap* out);
+// Scales or biases as uint16 [N][G], box `rows` rows x 8 values, unswizzled.
+bool encode_sb_map(const void* a, int64_t G, int64_t N, int rows, CUtensorMap* out);
 // Activations x [M][K] bfloat16 (16-byte aligned, K % 64 == 0) viewed as
 // [M][K/64][64], box 64 x (codes per chunk / 64) x 8 rows, 128-byte swizzle.
 bool encode_x_map(const void* x, int M, int64_t K, int group, int mb, CUtensorMap* out);

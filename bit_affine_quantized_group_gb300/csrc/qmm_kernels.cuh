@@ -96,8 +96,8 @@ template <int CAP>
 struct MainParams {
     MainHeader h;
     BankPtrs bank[CAP];
-    CUtensorMap tmw[CAP];   // packed codes: uint8 [N][row_bytes], box kTN x W, swizzled
-    CUtensorMap tms[CAP];   // scales: uint16 [N][G], box kTN x 8 (when sb_tma)
+    CUtensorMap tmw[CAP];   // packed codes: uint8 [N][row_bytes], box (block rows) x W, swizzled
+    CUtensorMap tms[CAP];   // scales: uint16 [N][G], box (block rows) x 8 (when sb_tma)
     CUtensorMap tmb[CAP];   // biases: same
     CUtensorMap tmx;        // activations: bf16 [M][K/64][64] (x rows in 64-code blocks), box 64 x CK/64 x 8
 };
@@ -116,12 +116,12 @@ struct ReduceParams {
 // ---------------------------------------------------------------------------
 // Work enumeration shared by every warp role. The flattened (bank, split, row)
 // space is cut evenly, in whole 16-row slabs, over the CTAs; a CTA's range is
-// cut at (bank, split) boundaries and then into row blocks of kTN rows (the
+// cut at (bank, split) boundaries and then into row blocks of TN rows (the
 // last one shorter); every row block walks the chunks of its K slice. One item = one chunk of one row block (for
 // the fused gate/up projection, each row block is walked for bank 0 (gate) and
 // then for bank 1 (up)).
 // ---------------------------------------------------------------------------
-template <bool SWIGLU>
+template <bool SWIGLU, int TN>
 struct WorkIter {
     int64_t r, r_end;       // flattened rows of this CTA still to start, end
     int64_t seg;            // bank * splits + split of the current segment
@@ -135,7 +135,7 @@ struct WorkIter {
 
     // The CTAs split the flattened rows on the 16-row slab grid (a CTA holds
     // whole slabs, the last one of the range possibly ragged), and a CTA walks
-    // its part of a segment in blocks of kTN rows (the last one shorter): the
+    // its part of a segment in blocks of TN rows (the last one shorter): the
     // consumers then compute few empty slab rows.
     __device__ __forceinline__ void init(const MainHeader& p) {
         const int64_t slabs = (p.rows_total + kSlab - 1) / kSlab;
@@ -150,7 +150,7 @@ struct WorkIter {
         seg_end = min(r_end, (seg + 1) * p.N);
         a0 = r;
         len = seg_end - r;
-        nb = static_cast<int>((len + kTN - 1) / kTN);
+        nb = static_cast<int>((len + TN - 1) / TN);
         ib = 0;
         pass = 0;
         split = static_cast<int>(seg % p.splits);
@@ -159,8 +159,8 @@ struct WorkIter {
         start_block(p);
     }
     __device__ __forceinline__ void start_block(const MainHeader& p) {
-        const int64_t a = a0 + static_cast<int64_t>(kTN) * ib;
-        const int64_t e = min(a0 + len, a + kTN);
+        const int64_t a = a0 + static_cast<int64_t>(TN) * ib;
+        const int64_t e = min(a0 + len, a + TN);
         n0 = a - seg * p.N;
         rows = static_cast<int>(e - a);
         bank = SWIGLU ? pass : static_cast<int>(seg / p.splits);
@@ -208,13 +208,13 @@ QMM_HD constexpr uint32_t f16_pow2_bits(int e) { return static_cast<uint32_t>(e 
 // Byte offset, inside a stage's weight tile, of byte b of tile row r (TMA box
 // layout with the W-byte swizzle: bits 4.. of the in-box address are XORed
 // with its bits 7..).
-template <int BITS, int GROUP>
+template <int BITS, int GROUP, int TN>
 __device__ __forceinline__ int wtile_off(int r, int b) {
     constexpr int W = wbox_width(BITS, GROUP);
     constexpr int LW = log2i(W);
     constexpr int MASK = W / 16 - 1;
     const int lin = r * W + (b & (W - 1));
-    return ((b >> LW) << (LW + 7)) + (lin ^ (((lin >> 7) & MASK) << 4));
+    return (b >> LW) * (W * TN) + (lin ^ (((lin >> 7) & MASK) << 4));   // box b / W holds TN rows
 }
 
 // ---------------------------------------------------------------------------
@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     static_assert(MB == 8 || LAY != kWide, "the wide consumer layout is for the 8-row kernel");
     constexpr int NCW = consumer_warps();
     constexpr int CPAR = consumer_parities(LAY);
+    constexpr int TN = consumer_rows(LAY);       // rows of a row block and of a weight stage
     constexpr int WPPC = NCW / CPAR;             // consumer warps of one parity
     constexpr int VB = vblocks_per_group(GROUP);
     constexpr int VPC = vblocks_per_chunk(GROUP);
@@ -235,15 +236,15 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     constexpr int RB = chunk_row_bytes(BITS, GROUP);
     constexpr int W = wbox_width(BITS, GROUP);
     constexpr int NBOX = wbox_count(BITS, GROUP);
-    constexpr int SWB = stage_weight_bytes(BITS, GROUP);
-    constexpr int SSB = stage_sb_bytes();
-    constexpr int WSB = wstage_bytes(BITS, GROUP);          // weight stage
+    constexpr int SWB = stage_weight_bytes(BITS, GROUP, LAY);
+    constexpr int SSB = stage_sb_bytes(LAY);
+    constexpr int WSB = wstage_bytes(BITS, GROUP, LAY);          // weight stage
     constexpr int ASB = aslot_bytes(GROUP, MB);             // activation slot
     constexpr int XRB = xraw_bytes(GROUP, MB);
     constexpr int NBX = CK / 64;                    // 64-code blocks per chunk
-    // weight stage: codes [NBOX][kTN][W] swizzled, then
-    constexpr int OFF_S = SWB;                      // scales [kTN][8] binary16
-    constexpr int OFF_B = OFF_S + SSB;              // biases [kTN][8] binary16
+    // weight stage: codes [NBOX][TN][W] swizzled, then
+    constexpr int OFF_S = SWB;                      // scales [TN][8] binary16
+    constexpr int OFF_B = OFF_S + SSB;              // biases [TN][8] binary16
     // activation slot:
     constexpr int XRT = XRB / NT;                   // raw x of one 8-row tile
     constexpr int OFF_XR = 0;                       // raw x [NT][8][NBX][128 B], 128-byte swizzle
@@ -309,8 +310,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 }
             }
         }
-        const uint32_t tx_stage = static_cast<uint32_t>(NBOX * kTN * W + (p.sb_tma ? 2 * SSB : 0));
-        WorkIter<SWIGLU> wi;
+        const uint32_t tx_stage = static_cast<uint32_t>(NBOX * TN * W + (p.sb_tma ? 2 * SSB : 0));
+        WorkIter<SWIGLU, TN> wi;
         wi.init(p);
         uint32_t it = 0;
         int slot = 0;             // it % S, kept incrementally
@@ -322,12 +323,12 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             if (wi.block_start()) {
                 // the cp.async path for scales/biases checks its buffers once per row block
                 sb_ok = p.sb_tma ||
-                    (wi.n0 >= 0 && wi.rows >= 1 && wi.rows <= kTN && wi.n0 + wi.rows <= p.N && wi.c0 >= 0 &&
+                    (wi.n0 >= 0 && wi.rows >= 1 && wi.rows <= TN && wi.n0 + wi.rows <= p.N && wi.c0 >= 0 &&
                      wi.c1 <= p.C && ((reinterpret_cast<uintptr_t>(bp.s) | reinterpret_cast<uintptr_t>(bp.b)) & 3) == 0);
                 if (!sb_ok && lane == 0) record_bad_copy(p.err, bp.s, static_cast<uint64_t>(wi.rows), 4u);
-                // the host gives a layout only row blocks it covers; a longer one
-                // would leave rows unwritten, so it is recorded
-                if (wi.rows > consumer_rows(LAY) && lane == 0)
+                // a row block longer than the layout covers would leave rows
+                // unwritten (the row blocks are cut to TN rows, so this never fires)
+                if (wi.rows > TN && lane == 0)
                     record_bad_copy(p.err, bp.w, static_cast<uint64_t>(wi.rows), 6u);
             }
             // After a timed-out wait the error is recorded and no further waits are
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 const int y = static_cast<int>(wi.n0);
 #pragma unroll
                 for (int bi = 0; bi < NBOX; ++bi)
-                    tma_load_2d(st + bi * (kTN * W), &P.tmw[wi.bank], wi.c * RB + bi * W, y, &wfull[slot], pol);
+                    tma_load_2d(st + bi * (TN * W), &P.tmw[wi.bank], wi.c * RB + bi * W, y, &wfull[slot], pol);
                 if (p.sb_tma) {
                     tma_load_2d(st + OFF_S, &P.tms[wi.bank], wi.c * kGPC, y, &wfull[slot], pol);
                     tma_load_2d(st + OFF_B, &P.tmb[wi.bank], wi.c * kGPC, y, &wfull[slot], pol);
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         constexpr int STRIDE = F <= SPT ? F : SPT;
         static_assert(F <= SPT || F % SPT == 0, "activation slot ownership");
         if (par >= STRIDE) return;
-        WorkIter<SWIGLU> lead;   // the item F ahead of the current one
+        WorkIter<SWIGLU, TN> lead;   // the item F ahead of the current one
         lead.init(p);
         uint32_t issued = 0;     // one past the last item whose raw copy this warp issued
         for (int i = 0; i < F && lead.valid; ++i, lead.next(p))
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         // warp exits.
         bool ok = true;
         uint32_t failed = 0;
-        WorkIter<SWIGLU> wi;
+        WorkIter<SWIGLU, TN> wi;
         wi.init(p);
 #pragma unroll 1
         for (int k = 0; k < par; ++k) {
@@ -679,13 +680,13 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 const int k = 2 * i + (lane >> 4);                       // 16-byte chunk (half block)
                 off[i] = lr * 128 + (((k & 7) ^ (lane & 7)) << 4);
             } else if constexpr (BITS == 2) {
-                off[i] = wtile_off<BITS, GROUP>(r0, 16 * i);
+                off[i] = wtile_off<BITS, GROUP, TN>(r0, 16 * i);
             } else {
                 const int vb = i >> 1;
                 const int b = vb * BB + 4 * ((BITS * t) >> 2) + 4 * (i & 1);
                 // 3-bit lane 3 needs no second word: read its first word again
                 const int bb = (BITS == 3 && t == 3 && (i & 1)) ? b - 4 : b;
-                off[i] = wtile_off<BITS, GROUP>(r0, bb);
+                off[i] = wtile_off<BITS, GROUP, TN>(r0, bb);
             }
         }
     }
@@ -702,7 +703,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     constexpr int NACC = CPAR == 1 ? 2 : 1;
     float acc[NACC][SPW][NT][4];
     uint32_t ipar = 0;        // item & 1
-    WorkIter<SWIGLU> wi;
+    WorkIter<SWIGLU, TN> wi;
     wi.init(p);
     for (; wi.valid; wi.next(p), ipar ^= 1u) {
         if (wi.block_start()) {
@@ -785,13 +786,13 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                         if constexpr (BITS == 4) {
                             // one ldmatrix per pair of blocks (rows r0 and r0 + 8 of both)
                             if constexpr ((vb & 1) == 0)
-                                ldmatrix_x4_at<(vb >> 3) * (kTN * 128) + SO>(cb[(vb >> 1) & 3], q4[sl][0], q4[sl][1],
+                                ldmatrix_x4_at<(vb >> 3) * (TN * 128) + SO>(cb[(vb >> 1) & 3], q4[sl][0], q4[sl][1],
                                                                              q4[sl][2], q4[sl][3]);
                             unpack4((vb & 1) ? q4[sl][2] : q4[sl][0], ra, magic);
                             unpack4((vb & 1) ? q4[sl][3] : q4[sl][1], rb, magic);
                         } else if constexpr (BITS == 8) {
                             uint32_t d0, d1, d2, d3;
-                            ldmatrix_x4_at<(vb >> 2) * (kTN * 128) + SO>(cb[vb & 3], d0, d1, d2, d3);
+                            ldmatrix_x4_at<(vb >> 2) * (TN * 128) + SO>(cb[vb & 3], d0, d1, d2, d3);
                             unpack8(d0, d2, ra, magic);
                             unpack8(d1, d3, rb, magic);
                         } else if constexpr (BITS == 2) {

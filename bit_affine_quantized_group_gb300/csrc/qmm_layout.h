@@ -60,8 +60,8 @@ QMM_HD constexpr int staging_warps(int mb) { return staging_per_tile(mb) * n8_ti
 //     the items in the stage slots of parity p (128 rows an item). It pays when
 //     a CTA's row blocks fill most of the 8 slabs and the pipeline keeps
 //     several stages per parity;
-//   * pair: one slab a warp in two parities (64 rows an item), two items in
-//     flight for CTAs of at most four slabs.
+//   * pair: one slab a warp in two parities, two items in flight; its row
+//     blocks (and weight stages) are 64 rows.
 // Every layout sums a block's even- and odd-index items apart and adds the two
 // at the end, so they all give the same bits.
 constexpr int kNarrow = 0;
@@ -70,7 +70,7 @@ constexpr int kPair = 2;
 QMM_HD constexpr int consumer_slabs(int lay) { return lay == kWide ? 2 : 1; }
 QMM_HD constexpr int consumer_parities(int lay) { return lay == kNarrow ? 1 : 2; }
 QMM_HD constexpr int consumer_warps() { return kSlabs; }
-// Rows of a row block the consumers cover (a CTA's blocks must not be longer).
+// Rows of a row block: the rows one work item covers.
 QMM_HD constexpr int consumer_rows(int lay) {
     return kSlab * consumer_slabs(lay) * consumer_warps() / consumer_parities(lay);
 }
@@ -111,12 +111,15 @@ QMM_HD constexpr int xstaged_bytes(int group, int mb) {
 // reads of 8 different rows fall in different banks); rows >= M arrive as zeros.
 QMM_HD constexpr int xraw_bytes(int group, int mb) { return 2 * chunk_codes(group) * mb; }
 
-// Weight stage (one chunk of one row block; 1024-byte aligned, the swizzle
-// atom): packed codes, scales, biases.
-QMM_HD constexpr int stage_weight_bytes(int bits, int group) { return kTN * chunk_row_bytes(bits, group); }
-QMM_HD constexpr int stage_sb_bytes() { return kTN * 16; }   // 8 binary16 values per row
-QMM_HD constexpr int wstage_bytes(int bits, int group) {
-    return round_up(stage_weight_bytes(bits, group) + 2 * stage_sb_bytes(), 1024);
+// Weight stage (one chunk of one row block of consumer_rows(lay) rows:
+// kTN, or 64 for the pair layout; 1024-byte aligned, the swizzle atom):
+// packed codes, scales, biases.
+QMM_HD constexpr int stage_weight_bytes(int bits, int group, int lay) {
+    return consumer_rows(lay) * chunk_row_bytes(bits, group);
+}
+QMM_HD constexpr int stage_sb_bytes(int lay) { return consumer_rows(lay) * 16; }   // 8 binary16 values per row
+QMM_HD constexpr int wstage_bytes(int bits, int group, int lay) {
+    return round_up(stage_weight_bytes(bits, group, lay) + 2 * stage_sb_bytes(lay), 1024);
 }
 // Activation slot (one chunk): raw activations (1024-byte aligned) and the
 // staged fragments.
@@ -134,7 +137,7 @@ QMM_HD constexpr int combine_bytes(int mb, int lay) {
 // more (staged, consumed), and the combine scratch. 1024 bytes of slack let the kernel align
 // its rings to 1024.
 QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int lay, int S, int F) {
-    return 1024 + S * wstage_bytes(bits, group) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
+    return 1024 + S * wstage_bytes(bits, group, lay) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
            combine_bytes(mb, lay);
 }
 // The most weight stages (<= kMaxStages) that fit kSmemOptin next to F

@@ -151,9 +151,11 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     mp.bank[0].s = scales_f16;
     mp.bank[0].b = biases_f16;
     mp.bank[0].out = out;
-    if (!encode_weight_map(packed_w, K, N, bits, group, &mp.tmw[0])) return QMM_ERR_CUDA;
+    const int rows = consumer_rows(lay);   // weight and scale boxes: one row block
+    if (!encode_weight_map(packed_w, K, N, bits, group, rows, &mp.tmw[0])) return QMM_ERR_CUDA;
     if (!encode_x_map(x_bf16, M, K, group, mb, &mp.tmx)) return QMM_ERR_CUDA;
-    if (h.sb_tma && (!encode_sb_map(scales_f16, h.G, N, &mp.tms[0]) || !encode_sb_map(biases_f16, h.G, N, &mp.tmb[0])))
+    if (h.sb_tma &&
+        (!encode_sb_map(scales_f16, h.G, N, rows, &mp.tms[0]) || !encode_sb_map(biases_f16, h.G, N, rows, &mp.tmb[0])))
         return QMM_ERR_CUDA;
 
     int64_t ctas = (h.rows_total + kSlab - 1) / kSlab;
