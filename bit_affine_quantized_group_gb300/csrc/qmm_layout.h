@@ -3,14 +3,14 @@
 //
 // Work decomposition (one main-kernel CTA per SM):
 //   * K is cut into chunks of kGPC = 8 scale groups. A CTA walks its rows in
-//     row blocks of up to kTN = 128 weight rows; one pipeline stage holds one
-//     chunk of one row block: the packed code bytes of those rows (TMA tensor
-//     boxes) and their 8 scales and 8 biases (TMA boxes). A separate ring of
-//     activation slots holds, per work item, the raw bfloat16 activation rows
-//     of the chunk (one TMA box per 8-row tile) and the chunk's staged
-//     activation fragments.
-//   * Warp roles: consumer_warps(MB) consumer warps (warp (w, p) owns
-//     consumer_slabs(MB) 16-row slabs of every row block, all 8 groups of
+//     row blocks of up to consumer_rows(layout) weight rows (kTN = 128, or 64
+//     in the pair layout); one pipeline stage holds one chunk of one row
+//     block: the packed code bytes of those rows (TMA tensor boxes) and their
+//     8 scales and 8 biases (TMA boxes). A separate ring of activation slots
+//     holds, per work item, the raw bfloat16 activation rows of the chunk (one
+//     TMA box per 8-row tile) and the chunk's staged activation fragments.
+//   * Warp roles: consumer_warps() consumer warps (warp (w, p) owns
+//     consumer_slabs(layout) 16-row slabs of every row block, all 8 groups of
 //     every chunk, in the stage slots of parity p when there are two consumer
 //     parities; the two parities' partial sums are added at the end of the row
 //     block), staging_warps(MB) activation-staging warps (warp (j, p) turns the
