@@ -156,12 +156,14 @@ QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, int lay, int
 }
 // Activation slots: a multiple of the consumer parities, and either at most
 // the staging warps per tile or a multiple of them (each warp owns whole
-// slots); the larger choice when it still leaves four weight stages.
+// slots). The 8-row kernel takes the larger choice that still leaves four
+// weight stages; the 16-row kernel, whose slots are twice as large, takes two
+// and gives the room to weight stages (measured faster than four slots).
 QMM_HD constexpr int act_slots(int bits, int group, int mb, int lay) {
     return mb == 8 ? (weight_stages_for(bits, group, mb, lay, 6) >= 4   ? 6
                       : weight_stages_for(bits, group, mb, lay, 4) >= 4 ? 4
                                                                          : 2)
-                   : (weight_stages_for(bits, group, mb, lay, 4) >= 4 ? 4 : 2);
+                   : 2;
 }
 QMM_HD constexpr int stage_count(int bits, int group, int mb, int lay) {
     return weight_stages_for(bits, group, mb, lay, act_slots(bits, group, mb, lay));
