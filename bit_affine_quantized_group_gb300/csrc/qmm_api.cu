@@ -14,6 +14,7 @@
 using namespace qmmk;
 
 static_assert(QMM_MAX_BANKS == kMaxBanks, "bank table size");
+static_assert(QMM_MAX_SPLITS == kMaxSplits, "K-slice bound table size");
 
 struct qmm_plan {
     qmm_desc d;
@@ -277,6 +278,7 @@ int forward_impl(const qmm_plan_t* p, const void* x_bf16, int M, int n_banks, co
     h.G = p->G;
     h.C = p->C;
     h.splits = p->splits;
+    set_slice_bounds(h);
     h.M = M;
     h.out_mode = p->splits > 1 ? kOutPartial : (p->d.out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
     h.sb_tma = (p->G % 8 == 0) ? 1 : 0;

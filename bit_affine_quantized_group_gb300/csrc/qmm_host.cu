@@ -140,6 +140,11 @@ bool encode_sb_map(const void* a, int64_t G, int64_t N, int rows, CUtensorMap* o
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+void set_slice_bounds(MainHeader& h) {
+    for (int s = 0; s <= kMaxSplits; ++s)
+        h.cb[s] = s <= h.splits ? static_cast<int>(static_cast<int64_t>(s) * h.C / h.splits) : h.C;
+}
+
 bool encode_x_map(const void* x, int M, int64_t K, int group, int mb, CUtensorMap* out) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr || M < 1 || K % 64 != 0) return false;

@@ -24,6 +24,9 @@ int consumer_layout(int bits, int group, int mb, int64_t rows_total, int64_t cta
 // 8-group chunks along K.
 int chunk_count(int64_t K, int group);
 
+// The chunk bounds of the header's K slices (h.cb, from h.C and h.splits).
+void set_slice_bounds(MainHeader& h);
+
 // Automatic K-slice count (1..cap) for `banks` projections of K x N in one
 // format on `num_sms` SMs, from a per-CTA cost model (see qmm_host.cu).
 int auto_split_count(int64_t K, int64_t N, int bits, int group, int64_t banks, int num_sms, int cap);

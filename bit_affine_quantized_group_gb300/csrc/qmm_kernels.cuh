@@ -61,6 +61,7 @@ __device__ __forceinline__ void static_for(F&& f) {
 }
 
 constexpr int kMaxBanks = 64;
+constexpr int kMaxSplits = 16;
 
 struct BankPtrs {
     const uint32_t* w;
@@ -84,6 +85,7 @@ struct MainHeader {
     int G;                  // K / group
     int C;                  // chunks = ceil(G / 8)
     int splits;
+    int cb[kMaxSplits + 1];   // first chunk of K slice s (s = 0..splits): s * C / splits
     int M;
     int out_mode;
     int sb_tma;             // scales/biases by TMA boxes (G % 8 == 0), else cp.async
@@ -116,54 +118,73 @@ struct ReduceParams {
 // ---------------------------------------------------------------------------
 // Work enumeration shared by every warp role. The flattened (bank, split, row)
 // space is cut evenly, in whole 16-row slabs, over the CTAs; a CTA's range is
-// cut at (bank, split) boundaries and then into row blocks of TN rows (the
-// last one shorter); every row block walks the chunks of its K slice. One item = one chunk of one row block (for
-// the fused gate/up projection, each row block is walked for bank 0 (gate) and
-// then for bank 1 (up)).
+// cut at (bank, split) boundaries (segments) and then into row blocks of TN
+// rows (the last one shorter); every row block walks the chunks of its K
+// slice. One item = one chunk of one row block (for the fused gate/up
+// projection, each row block is walked for bank 0 (gate) and then for bank 1
+// (up)).
 // ---------------------------------------------------------------------------
+
+// One CTA's share of the flattened rows: whole 16-row slabs (the last one of
+// the range possibly ragged), so the consumers compute few empty slab rows.
+// Computed once per CTA; the iterators of every warp role start from it and
+// then only step, with no division.
+struct CtaRange {
+    int64_t r, r_end;       // flattened rows [r, r_end)
+    int seg;                // segment of row r: bank * splits + split
+    int split, bank;        // seg % splits, seg / splits
+};
+__device__ __forceinline__ CtaRange cta_range(const MainHeader& p) {
+    const int64_t slabs = (p.rows_total + kSlab - 1) / kSlab;
+    CtaRange cr;
+    cr.r = min(p.rows_total, kSlab * (slabs * blockIdx.x / gridDim.x));
+    cr.r_end = min(p.rows_total, kSlab * (slabs * (blockIdx.x + 1) / gridDim.x));
+    cr.seg = static_cast<int>(cr.r / p.N);
+    cr.split = cr.seg % p.splits;
+    cr.bank = cr.seg / p.splits;
+    return cr;
+}
+
 template <bool SWIGLU, int TN>
 struct WorkIter {
     int64_t r, r_end;       // flattened rows of this CTA still to start, end
-    int64_t seg;            // bank * splits + split of the current segment
     int64_t seg_end;
     int64_t a0, len;        // first flattened row and length of the segment part
+    int seg;                // bank * splits + split of the current segment
+    int sbank;              // its bank
     int nb, ib;             // row blocks of the part, current one
     int pass;               // fused gate/up: 0 = gate, 1 = up
     int bank, split, rows, c0, c1, c;
     int64_t n0;             // first weight row of the current row block
     bool valid;
 
-    // The CTAs split the flattened rows on the 16-row slab grid (a CTA holds
-    // whole slabs, the last one of the range possibly ragged), and a CTA walks
-    // its part of a segment in blocks of TN rows (the last one shorter): the
-    // consumers then compute few empty slab rows.
-    __device__ __forceinline__ void init(const MainHeader& p) {
-        const int64_t slabs = (p.rows_total + kSlab - 1) / kSlab;
-        r = min(p.rows_total, kSlab * (slabs * blockIdx.x / gridDim.x));
-        r_end = min(p.rows_total, kSlab * (slabs * (blockIdx.x + 1) / gridDim.x));
+    __device__ __forceinline__ void init(const MainHeader& p, const CtaRange& cr) {
+        r = cr.r;
+        r_end = cr.r_end;
+        seg = cr.seg;
+        split = cr.split;
+        sbank = cr.bank;
         start_segment(p);
     }
     __device__ __forceinline__ void start_segment(const MainHeader& p) {
         valid = r < r_end;
         if (!valid) return;
-        seg = r / p.N;
-        seg_end = min(r_end, (seg + 1) * p.N);
+        seg_end = min(r_end, static_cast<int64_t>(seg + 1) * p.N);
         a0 = r;
         len = seg_end - r;
         nb = static_cast<int>((len + TN - 1) / TN);
         ib = 0;
         pass = 0;
-        split = static_cast<int>(seg % p.splits);
-        c0 = static_cast<int>(static_cast<int64_t>(split) * p.C / p.splits);
-        c1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.C / p.splits);
+        c0 = p.cb[split];
+        c1 = p.cb[split + 1];
         start_block(p);
     }
     __device__ __forceinline__ void start_block(const MainHeader& p) {
         const int64_t a = a0 + static_cast<int64_t>(TN) * ib;
         const int64_t e = min(a0 + len, a + TN);
-        n0 = a - seg * p.N;
+        n0 = a - static_cast<int64_t>(seg) * p.N;
         rows = static_cast<int>(e - a);
-        bank = SWIGLU ? pass : static_cast<int>(seg / p.splits);
+        bank = SWIGLU ? pass : sbank;
         c = c0;
     }
     __device__ __forceinline__ bool block_start() const { return c == c0; }
@@ -181,7 +202,14 @@ struct WorkIter {
             start_block(p);
             return;
         }
+        // the next segment starts where this one ended (seg_end = (seg + 1) * N
+        // unless the CTA's range ends first)
         r = seg_end;
+        ++seg;
+        if (++split == p.splits) {
+            split = 0;
+            ++sbank;
+        }
         start_segment(p);
     }
 };
@@ -272,8 +300,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     float* combine = reinterpret_cast<float*>(fempty + F);                 // [kSlabs][NT][4][32]
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    __shared__ CtaRange s_range;
 
     if (threadIdx.x == 0) {
+        s_range = cta_range(p);
         for (int i = 0; i < S; ++i) {
             // producer lane 0 (expect_tx), plus 32 cp.async arrivals when the
             // scales and biases come by cp.async
@@ -312,7 +342,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         }
         const uint32_t tx_stage = static_cast<uint32_t>(NBOX * TN * W + (p.sb_tma ? 2 * SSB : 0));
         WorkIter<SWIGLU, TN> wi;
-        wi.init(p);
+        wi.init(p, s_range);
         uint32_t it = 0;
         int slot = 0;             // it % S, kept incrementally
         uint32_t round = 0;       // it / S
@@ -444,7 +474,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         static_assert(F <= SPT || F % SPT == 0, "activation slot ownership");
         if (par >= STRIDE) return;
         WorkIter<SWIGLU, TN> lead;   // the item F ahead of the current one
-        lead.init(p);
+        lead.init(p, s_range);
         uint32_t issued = 0;     // one past the last item whose raw copy this warp issued
         for (int i = 0; i < F && lead.valid; ++i, lead.next(p))
             if (i % STRIDE == par) {
@@ -458,7 +488,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         bool ok = true;
         uint32_t failed = 0;
         WorkIter<SWIGLU, TN> wi;
-        wi.init(p);
+        wi.init(p, s_range);
 #pragma unroll 1
         for (int k = 0; k < par; ++k) {
             wi.next(p);
@@ -704,7 +734,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     float acc[NACC][SPW][NT][4];
     uint32_t ipar = 0;        // item & 1
     WorkIter<SWIGLU, TN> wi;
-    wi.init(p);
+    wi.init(p, s_range);
     for (; wi.valid; wi.next(p), ipar ^= 1u) {
         if (wi.block_start()) {
 #pragma unroll

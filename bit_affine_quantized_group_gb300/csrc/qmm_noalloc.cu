@@ -141,6 +141,7 @@ extern "C" int qmm_forward_noalloc(const void* x_bf16, int M, const uint32_t* pa
     h.G = static_cast<int>(K / group);
     h.C = C;
     h.splits = splits;
+    set_slice_bounds(h);
     h.M = M;
     h.out_mode = splits > 1 ? kOutPartial : (out_dtype == QMM_OUT_F32 ? kOutF32 : kOutBF16);
     h.sb_tma = (h.G % 8 == 0) ? 1 : 0;
