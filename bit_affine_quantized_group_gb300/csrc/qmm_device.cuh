@@ -20,7 +20,7 @@ constexpr uint32_t kErrBadCopy = 8u;      // a copy failed its bounds/alignment 
 
 // Record a rejected copy: error bit plus (first) offending address and size in
 // err[2..5]; the copy itself is skipped.
-__device__ __forceinline__ void record_bad_copy(uint32_t* err, const void* a, uint64_t b, uint32_t what) {
+static __device__ __noinline__ void record_bad_copy(uint32_t* err, const void* a, uint64_t b, uint32_t what) {
     if (atomicOr(err, kErrBadCopy) & kErrBadCopy) return;
     const uint64_t av = reinterpret_cast<uint64_t>(a);
     err[2] = static_cast<uint32_t>(av);

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     static_assert(XRT % 1024 == 0 && OFF_XT + 8 * MB <= ASB && OFF_B + SSB <= WSB, "stage layout");
     const MainHeader& p = P.h;
 
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
     // array so every access below stays a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     __shared__ CtaRange s_range;
+    static_assert(sizeof(CtaRange) <= kStaticSmem, "static shared memory");
 
     if (threadIdx.x == 0) {
         s_range = cta_range(p);
@@ -969,7 +970,16 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             }
         }
         if (cp == 0 && active) {
-            const BankPtrs bp = P.bank[wi.bank];
+            // this row block's outputs: [M][N] at column n0 of the bank's output
+            // (bf16 or fp32), or of its K slice's fp32 partial sums
+            const bool partial = p.out_mode == kOutPartial;
+            const bool to_bf16 = p.out_mode == kOutBF16;
+            void* const out = P.bank[wi.bank].out;
+            float* const fbase =
+                (partial ? p.partial + static_cast<int64_t>(wi.bank * p.splits + wi.split) * p.M * p.N
+                         : static_cast<float*>(out)) + wi.n0;
+            __nv_bfloat16* const hbase = static_cast<__nv_bfloat16*>(out) + wi.n0;
+            const int mrows = p.M;
 #pragma unroll
             for (int sl = 0; sl < SPW; ++sl) {
 #pragma unroll
@@ -978,31 +988,29 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 for (int hh = 0; hh < 2; ++hh) {
                     const int nl = r0 + kSlab * sl + 8 * hh;
                     if (nl >= wi.rows) continue;
-                    const int64_t n = wi.n0 + nl;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int mm = 8 * jj + 2 * t + e;
-                        if (mm >= p.M) continue;
+                        if (mm >= mrows) continue;
+                        const int64_t idx = static_cast<int64_t>(mm) * p.N + nl;
                         float v = acc[0][sl][jj][2 * hh + e];
-                        if (p.out_mode == kOutPartial) {
-                            p.partial[((static_cast<int64_t>(wi.bank) * p.splits + wi.split) * p.M + mm) * p.N + n] = v;
-                            continue;
-                        }
                         if constexpr (SWIGLU) {
-                            // gate pass: keep the fp32 gate; up pass: the same thread
-                            // wrote this (m, n) gate in the gate pass of this row block
-                            if (wi.bank == 0) {
-                                p.gate[mm * p.N + n] = v;
-                                continue;
+                            if (!partial) {
+                                // gate pass: keep the fp32 gate; up pass: the same thread
+                                // wrote this (m, n) gate in the gate pass of this row block
+                                float* const g = p.gate + wi.n0 + idx;
+                                if (wi.bank == 0) {
+                                    *g = v;
+                                    continue;
+                                }
+                                const float gv = *g;
+                                v = gv / (1.0f + expf(-gv)) * v;
                             }
-                            const float gv = p.gate[mm * p.N + n];
-                            v = gv / (1.0f + expf(-gv)) * v;
                         }
-                        if (p.out_mode == kOutF32) {
-                            static_cast<float*>(bp.out)[mm * p.N + n] = v;
-                        } else {
-                            static_cast<__nv_bfloat16*>(bp.out)[mm * p.N + n] = __float2bfloat16_rn(v);
-                        }
+                        if (to_bf16)
+                            hbase[idx] = __float2bfloat16_rn(v);
+                        else
+                            fbase[idx] = v;
                     }
                 }
             }

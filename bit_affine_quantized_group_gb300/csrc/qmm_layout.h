@@ -38,8 +38,12 @@ constexpr int kTN = 128;           // weight rows per row block
 constexpr int kSlab = 16;          // rows per MMA slab
 constexpr int kSlabs = kTN / kSlab; // 16-row slabs per row block
 constexpr int kMaxStages = 8;
-// Dynamic shared memory a CTA may opt into on sm_100-class GPUs (GB300: 227 KB).
-constexpr int kSmemOptin = 232448;
+// Shared memory a CTA may opt into on sm_100-class GPUs (GB300: 227 KB), and
+// the part of it the main kernel declares statically (its CTA's work range);
+// the dynamic part gets the rest.
+constexpr int kSmemOptinTotal = 232448;
+constexpr int kStaticSmem = 64;
+constexpr int kSmemOptin = kSmemOptinTotal - kStaticSmem;
 constexpr int kReduceThreads = 256;
 
 QMM_HD constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
