@@ -10,7 +10,7 @@ namespace qmmk {
 int stages_for(int bits, int group, int mb, int lay, int optin) {
     if (lay == kWide && mb != 8) return 0;
     const int st = stage_count(bits, group, mb, lay);
-    return (st >= 2 && main_smem_bytes(bits, group, mb, lay) + kStaticSmem <= optin) ? st : 0;
+    return (st >= 2 && main_smem_bytes(bits, group, mb, lay) <= optin) ? st : 0;
 }
 
 // The pair layout keeps two items in flight with one slab a warp, but covers

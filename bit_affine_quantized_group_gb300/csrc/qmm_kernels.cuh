@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     static_assert(XRT % 1024 == 0 && OFF_XT + 8 * MB <= ASB && OFF_B + SSB <= WSB, "stage layout");
     const MainHeader& p = P.h;
 
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned ring base, derived by pointer arithmetic on the shared
     // array so every access below stays a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     float* combine = reinterpret_cast<float*>(fempty + F);                 // [kSlabs][NT][4][32]
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    __shared__ CtaRange s_range;
-    static_assert(sizeof(CtaRange) <= kStaticSmem, "static shared memory");
+    CtaRange& s_range = *reinterpret_cast<CtaRange*>(reinterpret_cast<uint8_t*>(combine) + combine_bytes(MB, LAY));
+    static_assert(sizeof(CtaRange) <= kRangeBytes && alignof(CtaRange) <= 8, "work range area");
 
     if (threadIdx.x == 0) {
         s_range = cta_range(p);

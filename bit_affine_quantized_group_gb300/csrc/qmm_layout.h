@@ -38,12 +38,10 @@ constexpr int kTN = 128;           // weight rows per row block
 constexpr int kSlab = 16;          // rows per MMA slab
 constexpr int kSlabs = kTN / kSlab; // 16-row slabs per row block
 constexpr int kMaxStages = 8;
-// Shared memory a CTA may opt into on sm_100-class GPUs (GB300: 227 KB), and
-// the part of it the main kernel declares statically (its CTA's work range);
-// the dynamic part gets the rest.
-constexpr int kSmemOptinTotal = 232448;
-constexpr int kStaticSmem = 64;
-constexpr int kSmemOptin = kSmemOptinTotal - kStaticSmem;
+// Dynamic shared memory a CTA may opt into on sm_100-class GPUs (GB300: 227 KB).
+constexpr int kSmemOptin = 232448;
+// Bytes after the mbarriers and the combine scratch for the CTA's work range.
+constexpr int kRangeBytes = 32;
 constexpr int kReduceThreads = 256;
 
 QMM_HD constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -138,11 +136,11 @@ QMM_HD constexpr int combine_bytes(int mb, int lay) {
 // Dynamic shared memory of the main kernel with S weight stages and F
 // activation slots: the stages, the slots, two mbarriers per weight stage
 // (landed, consumed), per activation slot one per tile (raw landed) and two
-// more (staged, consumed), and the combine scratch. 1024 bytes of slack let the kernel align
-// its rings to 1024.
+// more (staged, consumed), the combine scratch and the CTA's work range.
+// 1024 bytes of slack let the kernel align its rings to 1024.
 QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int lay, int S, int F) {
     return 1024 + S * wstage_bytes(bits, group, lay) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
-           combine_bytes(mb, lay);
+           combine_bytes(mb, lay) + kRangeBytes;
 }
 // The most weight stages (<= kMaxStages) that fit kSmemOptin next to F
 // activation slots, a multiple of the consumer parities (each parity owns the
