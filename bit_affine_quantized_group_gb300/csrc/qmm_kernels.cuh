@@ -799,8 +799,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             uint4 q2a[SPW], q2b[SPW];   // 2-bit: the 16-byte chunk (two blocks) of rows r0, r0 + 8
             static_for<0, kGPC>([&](auto gq_c) {
                 constexpr int gq = decltype(gq_c)::value;
-                // the group's products, by k16 half of the blocks: two independent
-                // MMA chains a slab, added when the group is done
+                // the group's products. Groups of 32 (one k32 block): two independent
+                // MMAs a slab, one per k16 half, added when the group is done. Groups
+                // of 64: one chain of four MMAs a slab (measured faster there).
+                constexpr bool ONECHAIN = VB > 1;
                 float Pg[SPW][NT][2][4];
                 static_for<0, VB>([&](auto v_c) {
                     constexpr int v = decltype(v_c)::value;
@@ -849,7 +851,13 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                         }
                         static_for<0, NT>([&](auto j_c) {
                             constexpr int jj = decltype(j_c)::value;
-                            if constexpr (v == 0) {
+                            if constexpr (ONECHAIN) {
+                                if constexpr (v == 0)
+                                    mma_f16_zc(Pg[sl][jj][0], ra[0], rb[0], ra[1], rb[1], bf[jj].x, bf[jj].y);
+                                else
+                                    mma_f16(Pg[sl][jj][0], ra[0], rb[0], ra[1], rb[1], bf[jj].x, bf[jj].y);
+                                mma_f16(Pg[sl][jj][0], ra[2], rb[2], ra[3], rb[3], bf[jj].z, bf[jj].w);
+                            } else if constexpr (v == 0) {
                                 mma_f16_zc(Pg[sl][jj][0], ra[0], rb[0], ra[1], rb[1], bf[jj].x, bf[jj].y);
                                 mma_f16_zc(Pg[sl][jj][1], ra[2], rb[2], ra[3], rb[3], bf[jj].z, bf[jj].w);
                             } else {
@@ -869,8 +877,13 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                     for (int jj = 0; jj < NT; ++jj) {
                         // (elements 0, 1: row r0; 2, 3: row r0 + 8; paired by row)
                         float pg[4];
-                        add_x2(pg[0], pg[1], Pg[sl][jj][0][0], Pg[sl][jj][0][1], Pg[sl][jj][1][0], Pg[sl][jj][1][1]);
-                        add_x2(pg[2], pg[3], Pg[sl][jj][0][2], Pg[sl][jj][0][3], Pg[sl][jj][1][2], Pg[sl][jj][1][3]);
+                        if constexpr (ONECHAIN) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) pg[e] = Pg[sl][jj][0][e];
+                        } else {
+                            add_x2(pg[0], pg[1], Pg[sl][jj][0][0], Pg[sl][jj][0][1], Pg[sl][jj][1][0], Pg[sl][jj][1][1]);
+                            add_x2(pg[2], pg[3], Pg[sl][jj][0][2], Pg[sl][jj][0][3], Pg[sl][jj][1][2], Pg[sl][jj][1][3]);
+                        }
                         if constexpr (gq == 0) {
                             mul_x2(accc[sl][jj][0], accc[sl][jj][1], sa, sa, pg[0], pg[1]);
                             mul_x2(accc[sl][jj][2], accc[sl][jj][3], sb, sb, pg[2], pg[3]);
