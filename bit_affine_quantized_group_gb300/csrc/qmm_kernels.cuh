@@ -504,7 +504,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 failed = it;
             }
             uint8_t* st = aring + slot * ASB;
-            // refill the slot with the raw activations of the item F ahead
+            // refill the slot with the raw activations of the item F ahead (issued
+            // after the item is staged: a copy issued while the weight stages fill
+            // the copy engine can hold the warp, and the item F ahead is needed
+            // only F items later)
             auto refill = [&]() {
                 __syncwarp();
                 if (ok && lead.valid) {
@@ -555,7 +558,6 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             for (int w2 = VPC / 2; w2 >= 1; w2 /= 2)
 #pragma unroll
                 for (int i = 0; i < w2; ++i) bm[i] = bf16x2_absmax(bm[i], bm[i + w2]);
-            if constexpr (KEEP) refill();
             // the fragment area must be free: the consumers are done with the item F before
             if (it >= static_cast<uint32_t>(F))
                 mbar_wait_sleep(&fempty[slot], phase ^ 1u, p.err, kErrEmptyWait, 128u);
@@ -617,7 +619,6 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 mma_f16(Da, fr[0], 0u, fr[1], 0u, selq[q][0][0], selq[q][0][1]);
                 mma_f16(Da, fr[2], 0u, fr[3], 0u, selq[q][1][0], selq[q][1][1]);
             }
-            if constexpr (!KEEP) refill();
             // lane (g, t): groups t (half 0) and 4 + t (half 1) of row m
             const float xs0 = (D[0][0] + D[1][0]) * rf, xsc0 = (D[0][1] + D[1][1]) * (rf * 1024.0f);
             const float xs1 = (D[2][0] + D[3][0]) * rf, xsc1 = (D[2][1] + D[3][1]) * (rf * 1024.0f);
@@ -661,6 +662,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             // the warp's fragment stores, ordered by the warp barrier before one lane's release
             __syncwarp();
             if (lane == 0) mbar_arrive(&sfull[slot]);
+            refill();
 #pragma unroll 1
             for (int k = 0; k < STRIDE; ++k) {
                 wi.next(p);
