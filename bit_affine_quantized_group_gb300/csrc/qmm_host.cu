@@ -150,7 +150,10 @@ bool encode_x_map(const void* x, int M, int64_t K, int group, int mb, CUtensorMa
     if (enc == nullptr || M < 1 || K % 64 != 0) return false;
     const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(K / 64), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(chunk_codes(group) / 64), 8};   // one 8-row tile
+    // one 8-row tile; the 8-row kernel copies only the call's M rows (its rows >= M
+    // are never stored, and every row's staging and MMA column is its own)
+    const cuuint32_t rows = (mb == 8 && M < 8) ? static_cast<cuuint32_t>(M) : 8u;
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(chunk_codes(group) / 64), rows};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

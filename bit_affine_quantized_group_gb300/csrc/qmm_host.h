@@ -45,7 +45,8 @@ bool encode_weight_map(const void* w, int64_t K, int64_t N, int bits, int group,
 // Scales or biases as uint16 [N][G], box `rows` rows x 8 values, unswizzled.
 bool encode_sb_map(const void* a, int64_t G, int64_t N, int rows, CUtensorMap* out);
 // Activations x [M][K] bfloat16 (16-byte aligned, K % 64 == 0) viewed as
-// [M][K/64][64], box 64 x (codes per chunk / 64) x 8 rows, 128-byte swizzle.
+// [M][K/64][64], box 64 x (codes per chunk / 64) x 8 rows (M rows for the 8-row
+// kernel when M < 8), 128-byte swizzle.
 bool encode_x_map(const void* x, int M, int64_t K, int group, int mb, CUtensorMap* out);
 
 }  // namespace qmmk

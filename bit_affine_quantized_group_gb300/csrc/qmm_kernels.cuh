@@ -457,6 +457,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         // parity wait may only run one phase ahead of its barrier). x is read
         // only after the preceding work on the stream (which may have produced
         // it) has finished.
+        // bytes of one tile copy: the 8-row kernel copies only the call's M rows when
+        // M < 8 (rows M..7 of its raw area keep stale values; their fragments, sums
+        // and MMA columns are their own and are never stored)
+        const uint32_t xtile_bytes = static_cast<uint32_t>((MB == 8 ? min(p.M, 8) : 8) * NBX * 128);
         auto issue_raw = [&](int f, int c) {
             uint64_t* bar = &xfull[f * NT + j];
             if (c < 0 || c >= p.C) {
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 return;
             }
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(XRT));
+            mbar_arrive_expect_tx(bar, xtile_bytes);
             tma_load_3d(aring + f * ASB + OFF_XR + j * XRT, &P.tmx, 0, c * NBX, 8 * j, bar);
         };
         griddep_wait();
@@ -517,7 +521,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             };
             // Tile row g, 64-code block b: 128 bytes at u = g * NBX + b (times 128)
             // of the tile's raw area, with 16-byte piece c stored at piece c ^ (u & 7).
-            // Rows >= M and codes past K arrive from the TMA as zeros.
+            // Codes past K (and, in the 16-row kernel, rows >= M) arrive from the TMA
+            // as zeros.
             auto load_raw = [&](int vb, uint32_t (&v)[4]) {
                 const int u = g * NBX + (vb >> 1);
                 const uint8_t* rb = st + OFF_XR + j * XRT + u * 128;

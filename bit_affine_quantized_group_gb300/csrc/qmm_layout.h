@@ -110,7 +110,8 @@ QMM_HD constexpr int xstaged_bytes(int group, int mb) {
 // Raw activations of one chunk, per 8-row tile one 3-D TMA box of x viewed as
 // [M rows][K/64 blocks][64 codes]: [MB/8][8][chunk_codes/64][128 bytes], each
 // 128-byte line stored with the 128-byte swizzle (so the staging warps' 16-byte
-// reads of 8 different rows fall in different banks); rows >= M arrive as zeros.
+// reads of 8 different rows fall in different banks); the 16-row kernel's rows
+// >= M arrive as zeros, the 8-row kernel copies only M rows when M < 8.
 QMM_HD constexpr int xraw_bytes(int group, int mb) { return 2 * chunk_codes(group) * mb; }
 
 // Weight stage (one chunk of one row block of consumer_rows(lay) rows:
