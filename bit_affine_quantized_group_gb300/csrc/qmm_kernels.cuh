@@ -301,6 +301,11 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     CtaRange& s_range = *reinterpret_cast<CtaRange*>(reinterpret_cast<uint8_t*>(combine) + combine_bytes(MB, LAY));
+    // first activation copies issued (the producer of the wide layout with a full
+    // ring of small weight stages waits for them)
+    constexpr bool XFIRST = LAY == kWide && S >= kMaxStages;
+    uint64_t* const xissued =
+        reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(combine) + combine_bytes(MB, LAY) + kRangeBytes);
     static_assert(sizeof(CtaRange) <= kRangeBytes && alignof(CtaRange) <= 8, "work range area");
 
     if (threadIdx.x == 0) {
@@ -317,6 +322,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             mbar_init(&sfull[i], NT);             // one lane of the owning staging warp of each tile
             mbar_init(&fempty[i], WPPC);          // one lane of each of the slot parity's consumer warps
         }
+        // lane 0 of each staging warp that owns slots, once its first copies are issued
+        if constexpr (XFIRST) mbar_init(xissued, (F <= staging_per_tile(MB) ? F : staging_per_tile(MB)) * NT);
         fence_barrier_init();
     }
     __syncthreads();
@@ -364,6 +371,16 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             }
             // After a timed-out wait the error is recorded and no further waits are
             // made; the loop still runs to the end so that every warp finishes.
+            // In the wide layout with a full ring of small stages the producer,
+            // after the first stages, waits until the staging warps have issued
+            // their first activation copies (they do so once the preceding work
+            // has finished): those copies then queue ahead of the rest of the
+            // weight stream in the copy engine, and the first items are staged
+            // sooner (1-2 % faster calls on 5120 x 17408; the other layouts and
+            // rings of four large stages measured slower with the wait).
+            if (XFIRST && it == static_cast<uint32_t>(kStagesBeforeX) && ok &&
+                !mbar_wait(xissued, 0u, p.err, kErrEmptyWait))
+                ok = false;
             // (The slot's previous use was in round `round - 1`: parity round ^ 1.)
             if (it >= static_cast<uint32_t>(S) && ok &&
                 !mbar_wait_sleep(&wempty[slot], (round ^ 1u) & 1u, p.err, kErrEmptyWait, 128u))
@@ -486,6 +503,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 if (lane == 0) issue_raw(i, lead.c);
                 issued = static_cast<uint32_t>(i) + 1u;
             }
+        if (XFIRST && lane == 0) mbar_arrive(xissued);
 
         // After a timed-out wait no further copies are issued; the ones in
         // flight (this warp's items failed .. issued - 1) are drained before the

@@ -38,6 +38,9 @@ constexpr int kTN = 128;           // weight rows per row block
 constexpr int kSlab = 16;          // rows per MMA slab
 constexpr int kSlabs = kTN / kSlab; // 16-row slabs per row block
 constexpr int kMaxStages = 8;
+// Weight stages the producer issues before it lets the first activation copies
+// of the call go ahead of the rest (see the producer in qmm_kernels.cuh).
+constexpr int kStagesBeforeX = 2;
 // Dynamic shared memory a CTA may opt into on sm_100-class GPUs (GB300: 227 KB).
 constexpr int kSmemOptin = 232448;
 // Bytes after the mbarriers and the combine scratch for the CTA's work range.
@@ -137,11 +140,12 @@ QMM_HD constexpr int combine_bytes(int mb, int lay) {
 // Dynamic shared memory of the main kernel with S weight stages and F
 // activation slots: the stages, the slots, two mbarriers per weight stage
 // (landed, consumed), per activation slot one per tile (raw landed) and two
-// more (staged, consumed), the combine scratch and the CTA's work range.
+// more (staged, consumed), the combine scratch, the CTA's work range and one
+// more mbarrier (first activation copies issued).
 // 1024 bytes of slack let the kernel align its rings to 1024.
 QMM_HD constexpr int main_smem_bytes(int bits, int group, int mb, int lay, int S, int F) {
     return 1024 + S * wstage_bytes(bits, group, lay) + F * aslot_bytes(group, mb) + (2 * S + (2 + n8_tiles(mb)) * F) * 8 +
-           combine_bytes(mb, lay) + kRangeBytes;
+           combine_bytes(mb, lay) + kRangeBytes + 8;
 }
 // The most weight stages (<= kMaxStages) that fit kSmemOptin next to F
 // activation slots, a multiple of the consumer parities (each parity owns the
