@@ -975,6 +975,25 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             aslot = 0;
             aphase ^= 1u;
         }
+        if constexpr (CPAR == 2) {
+            // The next item is the other parity's. While it neither ends this row
+            // block nor is followed by a new one (and this item does not end the
+            // block either), step over it here: its slots and position only, not
+            // a whole visit of the loop.
+            if (mine && wi.c + 2 < wi.c1) {
+                wi.c += 1;        // the loop step adds the other one
+                ipar ^= 1u;
+                if (++cslot == S) {
+                    cslot = 0;
+                    cphase ^= 1u;
+                }
+                if (++aslot == F) {
+                    aslot = 0;
+                    aphase ^= 1u;
+                }
+                continue;
+            }
+        }
 
         if (!wi.block_end()) continue;
         if constexpr (NACC == 2) {
