@@ -187,6 +187,15 @@ struct WorkIter {
         bank = SWIGLU ? pass : sbank;
         c = c0;
     }
+    // k steps of next(): one add while they stay in the current row block (and pass)
+    __device__ __forceinline__ void advance(const MainHeader& p, int k) {
+        if (c + k < c1) {
+            c += k;
+            return;
+        }
+#pragma unroll 1
+        for (int i = 0; i < k; ++i) next(p);
+    }
     __device__ __forceinline__ bool block_start() const { return c == c0; }
     __device__ __forceinline__ bool block_end() const { return c == c1 - 1; }
     __device__ __forceinline__ void next(const MainHeader& p) {
@@ -512,10 +521,18 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         uint32_t failed = 0;
         WorkIter<SWIGLU, TN> wi;
         wi.init(p, s_range);
+        // (the 8-row kernel steps with one add inside a row block; the 16-row
+        // kernel, whose staging warps own every other item, measured faster
+        // stepping one item at a time)
+        if constexpr (MB == 8) {
+            wi.advance(p, par);
+            lead.advance(p, par);
+        } else {
 #pragma unroll 1
-        for (int k = 0; k < par; ++k) {
-            wi.next(p);
-            lead.next(p);
+            for (int k = 0; k < par; ++k) {
+                wi.next(p);
+                lead.next(p);
+            }
         }
         uint32_t it = static_cast<uint32_t>(par);
         for (; wi.valid; it += STRIDE) {
@@ -686,10 +703,15 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             __syncwarp();
             if (lane == 0) mbar_arrive(&sfull[slot]);
             refill();
+            if constexpr (MB == 8) {
+                wi.advance(p, STRIDE);
+                lead.advance(p, STRIDE);
+            } else {
 #pragma unroll 1
-            for (int k = 0; k < STRIDE; ++k) {
-                wi.next(p);
-                lead.next(p);
+                for (int k = 0; k < STRIDE; ++k) {
+                    wi.next(p);
+                    lead.next(p);
+                }
             }
         }
         if (!ok && lane == 0) {
