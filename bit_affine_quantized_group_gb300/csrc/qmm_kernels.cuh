@@ -683,15 +683,30 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                     lo[hv] = pack_half2(vl, wl);
                 }
             }
-#pragma unroll
-            for (int hv = 0; hv < 2; ++hv) {
+            // groups 4hv + t and 4hv + t + 1 form the bias fragment of lane (g, 2hv + t / 2),
+            // stored by the lanes with even t (with groups of 64 both halves' fragments
+            // behind one branch: 1.5-2.5 % faster calls than a branch per half, which
+            // measured 1 % faster with groups of 32)
+            auto bias_frag = [&](int hv) {
                 const uint32_t hi_p = __shfl_xor_sync(0xFFFFFFFFu, hi[hv], 1);
                 const uint32_t lo_p = __shfl_xor_sync(0xFFFFFFFFu, lo[hv], 1);
+                return make_uint4((hi[hv] & 0xFFFFu) | (hi_p << 16), (hi[hv] >> 16) | (hi_p & 0xFFFF0000u),
+                                  (lo[hv] & 0xFFFFu) | (lo_p << 16), (lo[hv] >> 16) | (lo_p & 0xFFFF0000u));
+            };
+            auto xb_at = [&](int hv) {
+                return reinterpret_cast<uint4*>(st + OFF_XB + (j * 32 + g * 4 + 2 * hv + (t >> 1)) * 16);
+            };
+            if constexpr (VB > 1) {
+                const uint4 b0 = bias_frag(0), b1 = bias_frag(1);
                 if ((t & 1) == 0) {
-                    // groups 4hv + t and 4hv + t + 1 form the bias fragment of lane (g, 2hv + t / 2)
-                    const uint4 frag = make_uint4((hi[hv] & 0xFFFFu) | (hi_p << 16), (hi[hv] >> 16) | (hi_p & 0xFFFF0000u),
-                                                  (lo[hv] & 0xFFFFu) | (lo_p << 16), (lo[hv] >> 16) | (lo_p & 0xFFFF0000u));
-                    *reinterpret_cast<uint4*>(st + OFF_XB + (j * 32 + g * 4 + 2 * hv + (t >> 1)) * 16) = frag;
+                    *xb_at(0) = b0;
+                    *xb_at(1) = b1;
+                }
+            } else {
+#pragma unroll
+                for (int hv = 0; hv < 2; ++hv) {
+                    const uint4 b = bias_frag(hv);
+                    if ((t & 1) == 0) *xb_at(hv) = b;
                 }
             }
             if (t == 0) {
