@@ -647,8 +647,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                             wi4 = cc >> 1;
                             hf = cc & 1;
                         }
-                        v2[e] = bf16_half(v[wi4], hf) * fs[rr][e];
+                        v2[e] = bf16_half(v[wi4], hf);
                     }
+                    // (f * 2^-j, exact: one paired multiply for the two codes)
+                    mul_x2(v2[0], v2[1], v2[0], v2[1], fs[rr][0], fs[rr][1]);
                     fr[rr] = f2_to_h2(v2[0], v2[1]);
                 }
                 *reinterpret_cast<uint4*>(st + OFF_XF + ((vb * NT + j) * 32 + lane) * 16) =
