@@ -797,10 +797,11 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
     // output is bitwise the same whether the 8- or the 16-row kernel made it.
     constexpr int NACC = CPAR == 1 ? 2 : 1;
     // With the 16-row tile (two activation slots) and in the pair layout a warp
-    // releases the stage and the slot as soon as it has loaded the bias-term
-    // operands, before the bias-term arithmetic, so the slot is restaged sooner
-    // (16-row calls 1.2-2 % faster, pr1_ref 1.3 %); with the 8-row tile's narrow
-    // and wide layouts that order measured up to 1.7 % slower.
+    // releases the activation slot with its last block's fragment loads and the
+    // stage once it has loaded the bias-term operands, before the last group's
+    // and the bias term's arithmetic, so the slot is restaged sooner (16-row calls
+    // 2-3.5 % faster, pr1_ref 1 %); with the 8-row tile's narrow and wide layouts
+    // the early stage release measured up to 1.7 % slower.
     constexpr bool EARLY_RELEASE = MB == 16 || LAY == kPair;
     float acc[NACC][SPW][NT][4];
     uint32_t ipar = 0;        // item & 1
@@ -872,6 +873,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                 for (int i = 0; i < NOFF; ++i) cb[i] = st + static_cast<uint32_t>(off[i]);
             }
             float accc[SPW][NT][4];
+            uint2 rfa[NT], sga[NT];   // bias-term operands from the slot (early release)
+            uint4 bba[NT];
             uint32_t q4[SPW][4];     // 4-bit: ldmatrix words of the current pair of blocks
             uint4 q2a[SPW], q2b[SPW];   // 2-bit: the 16-byte chunk (two blocks) of rows r0, r0 + 8
             static_for<0, kGPC>([&](auto gq_c) {
@@ -889,6 +892,18 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                         constexpr int jj = decltype(j_c)::value;
                         bf[jj] = lds128_at<OFF_XF + (vb * NT + jj) * 512>(b_l);
                     });
+                    if constexpr (EARLY_RELEASE && vb == VPC - 1) {
+                        // the slot's last reads (the bias-term operands with the last
+                        // block's fragments): one lane releases it after the warp barrier
+                        static_for<0, NT>([&](auto j_c) {
+                            constexpr int jj = decltype(j_c)::value;
+                            rfa[jj] = lds64_at<OFF_XT + 4 * (MB + 8 * jj)>(b_t);
+                            sga[jj] = lds64_at<OFF_XT + 4 * (8 * jj)>(b_t);
+                            bba[jj] = lds128_at<OFF_XB + jj * 512>(b_l);
+                        });
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&fempty[fslot]);
+                    }
                     static_for<0, SPW>([&](auto s_c) {
                         constexpr int sl = decltype(s_c)::value;
                         constexpr int SO = sl * kSlab * W;       // slab offset inside a weight box
@@ -1005,8 +1020,6 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             // (groups past the end of K, stale shared memory on the cp.async path: zeroed)
             if constexpr (EARLY_RELEASE) {
                 uint32_t av[SPW][4];
-                uint2 rfa[NT], sga[NT];
-                uint4 bba[NT];
                 static_for<0, SPW>([&](auto s_c) {
                     constexpr int sl = decltype(s_c)::value;
                     av[sl][0] = lds32_at<OFF_B + 256 * sl>(b_r0t) & keep;
@@ -1014,19 +1027,10 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
                     av[sl][2] = lds32_at<OFF_S + 256 * sl>(b_r0t) & keep;
                     av[sl][3] = lds32_at<OFF_S + 256 * sl + 128>(b_r0t) & keep;
                 });
-                static_for<0, NT>([&](auto j_c) {
-                    constexpr int jj = decltype(j_c)::value;
-                    rfa[jj] = lds64_at<OFF_XT + 4 * (MB + 8 * jj)>(b_t);
-                    sga[jj] = lds64_at<OFF_XT + 4 * (8 * jj)>(b_t);
-                    bba[jj] = lds128_at<OFF_XB + jj * 512>(b_l);
-                });
-                // every value the warp reads from the stage and the slot is loaded:
-                // after the warp barrier one lane releases both
+                // every value the warp reads from the stage is loaded: after the warp
+                // barrier one lane releases it (the slot is released already)
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&wempty[slot]);
-                    mbar_arrive(&fempty[fslot]);
-                }
+                if (lane == 0) mbar_arrive(&wempty[slot]);
                 released = true;
                 static_for<0, SPW>([&](auto s_c) {
                     constexpr int sl = decltype(s_c)::value;
