@@ -40,7 +40,7 @@ cudaError_t launch_one(const LaunchCfg& L, const MainParams<CAP>& mp) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(L.ctas));
-    cfg.blockDim = dim3(main_threads(MB));
+    cfg.blockDim = dim3(main_threads(MB, GROUP, LAY));
     cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
     cfg.stream = L.stream;
     cfg.attrs = attr;

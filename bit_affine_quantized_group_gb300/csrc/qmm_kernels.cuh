@@ -258,9 +258,9 @@ __device__ __forceinline__ int wtile_off(int r, int b) {
 // The main kernel.
 // ---------------------------------------------------------------------------
 template <int BITS, int GROUP, int MB, int CAP, int LAY>
-__global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
+__global__ void __launch_bounds__(main_threads(MB, GROUP, LAY), 1) qmm_main_kernel(const __grid_constant__ MainParams<CAP> P) {
     constexpr int NT = n8_tiles(MB);
-    constexpr int NSW = staging_warps(MB);
+    constexpr int NSW = staging_warps(MB, GROUP, LAY);
     static_assert(MB == 8 || LAY != kWide, "the wide consumer layout is for the 8-row kernel");
     constexpr int NCW = consumer_warps();
     constexpr int CPAR = consumer_parities(LAY);
@@ -332,7 +332,8 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
             mbar_init(&fempty[i], WPPC);          // one lane of each of the slot parity's consumer warps
         }
         // lane 0 of each staging warp that owns slots, once its first copies are issued
-        if constexpr (XFIRST) mbar_init(xissued, (F <= staging_per_tile(MB) ? F : staging_per_tile(MB)) * NT);
+        if constexpr (XFIRST)
+            mbar_init(xissued, (F <= staging_per_tile(MB, GROUP, LAY) ? F : staging_per_tile(MB, GROUP, LAY)) * NT);
         fence_barrier_init();
     }
     __syncthreads();
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(main_threads(MB), 1) qmm_main_kernel(const __g
         // m = 8j + g and, in each k32 block, the 8 codes it holds in the
         // consumers' fragments. Everything it needs across lanes (the row's
         // largest |x| and the bias-term range) reduces inside the quad.
-        constexpr int SPT = staging_per_tile(MB);
+        constexpr int SPT = staging_per_tile(MB, GROUP, LAY);
         const int sw = warp - NCW;
         const int j = sw / SPT;
         const int par = sw % SPT;

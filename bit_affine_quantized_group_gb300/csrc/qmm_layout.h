@@ -13,7 +13,7 @@
 //     consumer_slabs(layout) 16-row slabs of every row block, all 8 groups of
 //     every chunk, in the stage slots of parity p when there are two consumer
 //     parities; the two parities' partial sums are added at the end of the row
-//     block), staging_warps(MB) activation-staging warps (warp (j, p) turns the
+//     block), staging_warps activation-staging warps (warp (j, p) turns the
 //     raw activations of 8-row tile j into tensor-core fragments in the
 //     activation slots it owns) and one weight-copy-issuing producer warp.
 //   * Inside a slab the contraction runs on tensor cores with
@@ -52,13 +52,7 @@ QMM_HD constexpr int log2i(int v) { return v <= 1 ? 0 : 1 + log2i(v / 2); }
 
 // 8-row activation tiles of an MB-row kernel (MB = 8 or 16).
 QMM_HD constexpr int n8_tiles(int mb) { return mb / 8; }
-// Staging warps: staging_per_tile(mb) per 8-row activation tile, warp p of a
-// tile owning the activation slots s with s % staging_per_tile == p.
-QMM_HD constexpr int staging_per_tile(int mb) { return mb == 8 ? 6 : 2; }
-QMM_HD constexpr int staging_warps(int mb) { return staging_per_tile(mb) * n8_tiles(mb); }
-// Consumer warps, in one of three layouts, 8 warps each (with the staging
-// warps and the producer at most four warps share a scheduler: 128 registers a
-// thread):
+// Consumer warps, in one of three layouts, 8 warps each:
 //   * narrow: one 16-row slab a warp, every work item (128 rows an item);
 //   * wide (8-row kernel only): two slabs a warp (two independent MMA chains
 //     sharing the activation fragment loads) in two parities, parity p taking
@@ -79,7 +73,27 @@ QMM_HD constexpr int consumer_warps() { return kSlabs; }
 QMM_HD constexpr int consumer_rows(int lay) {
     return kSlab * consumer_slabs(lay) * consumer_warps() / consumer_parities(lay);
 }
-QMM_HD constexpr int main_threads(int mb) { return (consumer_warps() + staging_warps(mb) + 1) * 32; }
+// Staging warps: staging_per_tile per 8-row activation tile, warp p of a tile
+// owning the activation slots s with s % staging_per_tile == p. The 8-row
+// kernel takes six, or three in the wide layout with groups of 32: there the raw
+// activations of a chunk stay in registers between the staging passes, three
+// warps keep up with the consumers, and a CTA of 12 warps (three a scheduler)
+// leaves 168 registers a thread instead of 128 (5120 x 17408 calls at 8 rows
+// 0.8 % faster with 4-bit codes, 2.7 % with 5-bit, 6.7 % with 6-bit; with groups
+// of 64 and in the other layouts three staging warps measured 1-15 % slower).
+// The 16-row kernel takes two per tile.
+QMM_HD constexpr int staging_per_tile(int mb, int group, int lay) {
+    return mb == 8 ? (group == 32 && lay == kWide ? 3 : 6) : 2;
+}
+QMM_HD constexpr int staging_warps(int mb, int group, int lay) {
+    return staging_per_tile(mb, group, lay) * n8_tiles(mb);
+}
+QMM_HD constexpr int main_threads(int mb, int group, int lay) {
+    return (consumer_warps() + staging_warps(mb, group, lay) + 1) * 32;
+}
+// F activation slots suit spt staging warps a tile when every warp owns whole
+// slots: F at most spt, or a multiple of it.
+QMM_HD constexpr bool slots_fit(int f, int spt) { return f <= spt || f % spt == 0; }
 
 // k32 blocks per scale group and per chunk.
 QMM_HD constexpr int vblocks_per_group(int group) { return group / 32; }
@@ -167,9 +181,10 @@ QMM_HD constexpr int weight_stages_for(int bits, int group, int mb, int lay, int
 // weight stages; the 16-row kernel, whose slots are twice as large, takes two
 // and gives the room to weight stages (measured faster than four slots).
 QMM_HD constexpr int act_slots(int bits, int group, int mb, int lay) {
-    return mb == 8 ? (weight_stages_for(bits, group, mb, lay, 6) >= 4   ? 6
-                      : weight_stages_for(bits, group, mb, lay, 4) >= 4 ? 4
-                                                                         : 2)
+    return mb == 8 ? (weight_stages_for(bits, group, mb, lay, 6) >= 4 ? 6
+                      : weight_stages_for(bits, group, mb, lay, 4) >= 4 && slots_fit(4, staging_per_tile(mb, group, lay))
+                          ? 4
+                          : 2)
                    : 2;
 }
 QMM_HD constexpr int stage_count(int bits, int group, int mb, int lay) {
