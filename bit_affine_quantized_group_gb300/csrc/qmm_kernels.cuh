@@ -803,7 +803,9 @@ __global__ void __launch_bounds__(main_threads(MB, GROUP, LAY), 1) qmm_main_kern
     // and the bias term's arithmetic, so the slot is restaged sooner (16-row calls
     // 2-3.5 % faster, pr1_ref 1 %); with the 8-row tile's narrow and wide layouts
     // the early stage release measured up to 1.7 % slower.
-    constexpr bool EARLY_RELEASE = MB == 16 || LAY == kPair;
+    // (Not the fused gate/up kernel: there the early order spills and its 16-row
+    // calls measured 3 % slower.)
+    constexpr bool EARLY_RELEASE = (MB == 16 && !SWIGLU) || LAY == kPair;
     float acc[NACC][SPW][NT][4];
     uint32_t ipar = 0;        // item & 1
     WorkIter<SWIGLU, TN> wi;
